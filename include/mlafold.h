@@ -1,0 +1,167 @@
+/*
+ * mlafold.h -- C ABI of the folded, KV-balanced FP8 MLA decode for GB300 (sm_103a).
+ *
+ * What the library computes (pages: "vllm...specialized_decode.drafter.attention",
+ * module overview and `folded_decode`; "vllm...specialized_decode.cutedsl.mla.balanced",
+ * module overview and `BalancedMla.plan` / `BalancedMla.decode`):
+ *
+ *   Absorbed Multi-head Latent Attention decode is MQA over one shared latent
+ *   KV head of 576 dims (512 latent + 64 rope); the value is the 512-dim latent
+ *   slice of the same cache row. The k query tokens of a non-causal draft block
+ *   are folded into the head axis, [R*k, H, 576] -> [R, k*H, 576], so each
+ *   request's cache is read once instead of k times. Every one of the M = k*H
+ *   (token, head) rows of request r gets its own softmax over keys
+ *   j < seq_lens[r]:
+ *
+ *     s[m][j]  = bmm1_scale * dot(q[r][m][0:576], kv[page(r,j)][j%64][0:576])
+ *     out[r][m] = bmm2_scale * sum_j softmax_j(s[m]) * kv[page(r,j)][j%64][0:512]
+ *     lse[r][m] = log2 sum_j 2^(s[m][j] * log2(e))         (base-2 LSE)
+ *
+ *   with page(r, j) = block_table[r][j / 64]. bmm1_scale = sm_scale * q_scale *
+ *   kv_scale and bmm2_scale = kv_scale are the stock decode's scales
+ *   (drafter-attention page, `_scales`). Folded and stock layouts are the same
+ *   memory: row m = t*H + h of request r is token r*k + t, head h.
+ *
+ * Pipeline per decode step: mla_plan_splits (once per step, reused by every
+ * layer) -> mla_folded_decode (per layer) -> mla_split_combine (per layer).
+ *
+ * Conventions for every entry point:
+ *   - The caller owns all memory and the stream. The library never allocates
+ *     device memory, never synchronises the stream and never frees.
+ *   - Device pointers must point to memory of the current CUDA device. Calls
+ *     are asynchronous on `stream` (NULL = the legacy default stream).
+ *   - Arguments are validated on the host before any launch; a bad argument
+ *     returns a negative mla_status and launches nothing. No C++ exception
+ *     crosses the ABI and nothing aborts the process.
+ *   - A launch failure returns MLA_ERR_CUDA (the CUDA error is left for the
+ *     caller to read with cudaGetLastError).
+ *   - Kernels are chained with programmatic dependent launch: each reads its
+ *     predecessor's outputs only after the grid dependency is resolved.
+ *   - Nothing is prepared lazily at call time beyond host-side descriptor
+ *     encoding, so the calls can be captured into a CUDA graph once the
+ *     buffers exist (the pages prepare their plans before capture:
+ *     balanced-MLA page, `BalancedMla.require`).
+ */
+#ifndef MLAFOLD_H
+#define MLAFOLD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle: pass a cudaStream_t (or NULL). */
+typedef struct CUstream_st *mla_stream_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_NULL = -1,        /* a required pointer is NULL                        */
+  MLA_ERR_SHAPE = -2,       /* a size is out of range (see mla_shape)            */
+  MLA_ERR_WORKSPACE = -3,   /* workspace_bytes < mla_workspace_bytes()          */
+  MLA_ERR_LIST = -4,        /* list_len < mla_plan_list_len()                    */
+  MLA_ERR_UNSUPPORTED = -5, /* page_size != 64, or the device is not sm_103      */
+  MLA_ERR_CUDA = -6,        /* a CUDA runtime or driver call failed              */
+  MLA_ERR_ALIGN = -7        /* a pointer is not aligned as documented            */
+} mla_status;
+
+typedef enum {
+  /* Split counts planned from the KV lengths: the longest requests split the
+   * most, so one wave of persistent CTAs finishes together (balanced-MLA page,
+   * module overview). */
+  MLA_POLICY_BALANCED = 0,
+  /* Every request gets the same split count, fixed by the batch shape
+   * (the uniform tokenspeed schedule the balanced-MLA page compares against). */
+  MLA_POLICY_UNIFORM = 1
+} mla_policy;
+
+/* Problem shape and plan parameters. All fields are host values. */
+typedef struct {
+  int32_t R;                /* requests in the batch, 1..1024                              */
+  int32_t k;                /* query tokens per request (draft block), >= 1                */
+  int32_t H;                /* heads per token, >= 1; M = k*H rows per request, <= 4096    */
+  int32_t page_size;        /* tokens per cache page; must be 64                           */
+  int32_t max_pages;        /* entries per block_table row (row pitch), >= 1               */
+  int32_t num_pages;        /* pages in the cache, >= 1, < 2^25                            */
+  int32_t num_ctas;         /* persistent CTAs the plan targets and the decode launches;
+                               normally the device's SM count, 1..65535                    */
+  int32_t min_split_tokens; /* smallest split a long request is cut into, >= 1 (e.g. 256)  */
+  int32_t max_splits;       /* largest split count of one request, 1..4096 (e.g. 64)       */
+  int32_t policy;           /* mla_policy                                                   */
+} mla_shape;
+
+/* Capacity, in entries, of the work list `work` that mla_plan_splits fills
+ * for this shape: enough for any length vector. Returns the capacity (>= 1)
+ * or a negative mla_status. Host only; launches nothing. */
+int32_t mla_plan_list_len(const mla_shape *shape);
+
+/* Bytes of split-KV workspace mla_folded_decode and mla_split_combine need for
+ * this shape: FP32 partial outputs [slots][M][512] followed by FP32 log2 LSEs
+ * [slots][M], where `slots` bounds the work items of requests that get two or
+ * more splits (the pages size the same thing as rows x splits x heads x
+ * (512 + 1) x 4 bytes: drafter-attention page, `tier_workspace_bytes`).
+ * Writes the size to *bytes (0 when no request can be split). Host only. */
+int32_t mla_workspace_bytes(const mla_shape *shape, size_t *bytes);
+
+/* Plan the step's splits on the device (one CTA), from the KV lengths.
+ *   seq_lens [R] int32, device: keys per request (negative is read as 0).
+ *   counts   [R] int32, device, written: splits of each request (>= 1).
+ *   work     [list_len] int32, device, written: items (request << 12 | split),
+ *            requests longest first (ties: lower index first), splits in
+ *            ascending order, then -1 to the end.
+ *   list_len must be >= mla_plan_list_len(shape).
+ * Integer arithmetic only; the result is a pure function of the lengths and
+ * the shape (the project's CPU planner reproduces it bit for bit). */
+int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t *counts,
+                        int32_t *work, int32_t list_len, mla_stream_t stream);
+
+/* Split-KV decode of the planned work list.
+ *   q           [R*k, H, 576] FP8 E4M3, device, 16-byte aligned: the queries in the
+ *               stock token-major layout (= the folded [R, M, 576] view).
+ *   kv          [num_pages, 64, 576] FP8 E4M3, device, 16-byte aligned: the
+ *               paged latent cache (cols 0..511 latent = value, 512..575 rope).
+ *   block_table [R, max_pages] int32, device: page ids; only the first
+ *               ceil(seq_lens[r] / 64) entries of row r are read.
+ *   seq_lens    [R] int32, device: the same lengths that were planned.
+ *   bmm1_scale  sm_scale * q_scale * kv_scale; bmm2_scale: kv_scale.
+ *   counts/work the plan of mla_plan_splits for these lengths; list_len its size.
+ *   workspace   >= mla_workspace_bytes(shape) bytes, device, 256-byte aligned;
+ *               scratch for split partials (contents need not be initialised).
+ *   out         [R, M, 512] BF16, device, 16-byte aligned, written for requests
+ *               with one split (the others are written by mla_split_combine).
+ *   lse         [R, M] FP32 base-2 LSE, device, written like `out`.
+ *   status      optional int32 device word (may be NULL); the kernel ORs in
+ *               MLA_FAULT_* bits for conditions it detects instead of trapping.
+ * Numerics: FP8 QK^T and PV on the tensor cores with FP32 accumulation; FP32
+ * online softmax in base 2 whose running max is kept while a new score
+ * exceeds it by at most 8 (2^8, balanced-MLA page, module overview); P is fed
+ * to the PV product as FP8 E4M3, unscaled, as the sum of two E4M3 terms
+ * (hi = e4m3(p), lo = e4m3(p - hi)); the normaliser is the FP32 sum of p. */
+int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          float bmm1_scale, float bmm2_scale, const int32_t *counts,
+                          const int32_t *work, int32_t list_len, void *workspace,
+                          size_t workspace_bytes, void *out, float *lse, int32_t *status,
+                          mla_stream_t stream);
+
+/* LSE reduction of the split partials into `out` and `lse` for the requests
+ * with two or more splits: out = bmm2_scale * sum_s w_s O_s / sum_s w_s, with
+ * w_s = 2^(lse_s - max_s lse_s), rounded once to BF16; lse = max + log2 sum w
+ * (drafter-attention page, `DraftDcp`: exp2(lse - max) / sum in FP32, one
+ * BF16 rounding). Arguments as for mla_folded_decode, same plan and workspace.
+ * Rows whose splits are all empty get out = 0 and lse = -inf. */
+int32_t mla_split_combine(const mla_shape *shape, const int32_t *counts, const int32_t *work,
+                          int32_t list_len, const void *workspace, size_t workspace_bytes,
+                          float bmm2_scale, void *out, float *lse, mla_stream_t stream);
+
+/* Bits the decode kernel ORs into *status. */
+#define MLA_FAULT_WAIT_TIMEOUT 0x1 /* a pipeline wait gave up; the CTA stopped early */
+#define MLA_FAULT_PAGE_RANGE 0x2   /* a block-table entry was outside [0, num_pages) */
+#define MLA_FAULT_WORK_ITEM 0x4    /* a work item named a request or split out of range */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLAFOLD_H */

@@ -1,0 +1,131 @@
+"""Folded, KV-balanced FP8 MLA decode for GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``include/mlafold.h``: it marshals
+PyTorch device tensors into pointers and calls the library; every step of the
+decode runs in the library's CUDA kernels. PyTorch only owns the memory and
+the stream.
+
+The API follows the pages (drafter-attention page, ``folded_decode``;
+balanced-MLA page, ``BalancedMla.require`` / ``plan`` / ``decode``):
+
+* ``FoldedMla(R, k, H, max_pages, num_pages, device)`` allocates the plan
+  buffers (``counts`` zeros, ``work`` -1) and the split-KV workspace up front,
+  so nothing is allocated later (and a CUDA graph can capture the calls);
+* ``.plan(seq_lens)`` plans the step's splits on the device, once per step;
+* ``.decode(q, kv, block_table, seq_lens, bmm1_scale, bmm2_scale)`` runs the
+  split-KV decode and the LSE reduction: BF16 ``out [R, k*H, 512]`` and the
+  base-2 ``lse [R, k*H]``, in the stock token-major-then-head order.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (FAULT_PAGE_RANGE, FAULT_WAIT_TIMEOUT, FAULT_WORK_ITEM, MlaError, MlaShape,
+                   POLICY_BALANCED, POLICY_UNIFORM)
+
+__all__ = ["MlaShape", "MlaError", "POLICY_BALANCED", "POLICY_UNIFORM", "make_shape",
+           "plan_list_len", "workspace_bytes", "plan_splits", "folded_decode",
+           "split_combine", "FoldedMla", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
+           "FAULT_WORK_ITEM", "library_path"]
+
+PAGE = 64
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def make_shape(R: int, k: int, H: int, max_pages: int, num_pages: int, num_ctas: int,
+               min_split_tokens: int = 256, max_splits: int = 64,
+               policy: int = POLICY_BALANCED) -> MlaShape:
+    return MlaShape(R, k, H, PAGE, max_pages, num_pages, num_ctas, min_split_tokens,
+                    max_splits, policy)
+
+
+def plan_list_len(shape: MlaShape) -> int:
+    return _lib.check("mla_plan_list_len", _lib.load().mla_plan_list_len(ctypes.byref(shape)))
+
+
+def workspace_bytes(shape: MlaShape) -> int:
+    out = ctypes.c_size_t(0)
+    _lib.check("mla_workspace_bytes", _lib.load().mla_workspace_bytes(ctypes.byref(shape),
+                                                                      ctypes.byref(out)))
+    return out.value
+
+
+def plan_splits(shape: MlaShape, seq_lens, counts, work, stream=None) -> None:
+    _lib.check("mla_plan_splits", _lib.load().mla_plan_splits(
+        ctypes.byref(shape), _ptr(seq_lens), _ptr(counts), _ptr(work), work.numel(),
+        _stream(stream)))
+
+
+def folded_decode(shape: MlaShape, q, kv, block_table, seq_lens, bmm1_scale: float,
+                  bmm2_scale: float, counts, work, workspace, out, lse, status=None,
+                  stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.check("mla_folded_decode", _lib.load().mla_folded_decode(
+        ctypes.byref(shape), _ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens),
+        float(bmm1_scale), float(bmm2_scale), _ptr(counts), _ptr(work), work.numel(),
+        _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))
+
+
+def split_combine(shape: MlaShape, counts, work, workspace, bmm2_scale: float, out, lse,
+                  stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.check("mla_split_combine", _lib.load().mla_split_combine(
+        ctypes.byref(shape), _ptr(counts), _ptr(work), work.numel(), _ptr(workspace), ws_bytes,
+        float(bmm2_scale), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+class FoldedMla:
+    """Plan buffers and split-KV workspace of one decode shape.
+
+    Everything is allocated here, before any capture; ``plan`` and ``decode``
+    only launch kernels (balanced-MLA page, ``BalancedMla.require``: prepared
+    before capture, one shared scratch)."""
+
+    def __init__(self, R: int, k: int, H: int, max_pages: int, num_pages: int,
+                 device=None, num_ctas: int | None = None, min_split_tokens: int = 256,
+                 max_splits: int = 64, policy: int = POLICY_BALANCED):
+        self.device = torch.device(device if device is not None else "cuda")
+        if num_ctas is None:
+            num_ctas = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self.shape = make_shape(R, k, H, max_pages, num_pages, num_ctas, min_split_tokens,
+                                max_splits, policy)
+        self.R, self.k, self.H, self.M = R, k, H, k * H
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.counts = torch.zeros(R, **i32)
+        self.work = torch.full((plan_list_len(self.shape),), -1, **i32)
+        self.workspace = torch.empty(max(workspace_bytes(self.shape), 256), dtype=torch.uint8,
+                                     device=self.device)
+        self.status = torch.zeros(1, **i32)
+
+    def plan(self, seq_lens, stream=None) -> None:
+        plan_splits(self.shape, seq_lens, self.counts, self.work, stream)
+
+    def decode(self, q, kv, block_table, seq_lens, bmm1_scale: float, bmm2_scale: float,
+               out=None, lse=None, stream=None):
+        if out is None:
+            out = torch.empty((self.R, self.M, 512), dtype=torch.bfloat16, device=self.device)
+        if lse is None:
+            lse = torch.empty((self.R, self.M), dtype=torch.float32, device=self.device)
+        folded_decode(self.shape, q, kv, block_table, seq_lens, bmm1_scale, bmm2_scale,
+                      self.counts, self.work, self.workspace, out, lse, self.status, stream)
+        split_combine(self.shape, self.counts, self.work, self.workspace, bmm2_scale, out, lse,
+                      stream)
+        return out, lse

@@ -1,0 +1,93 @@
+// Shared constants, plan arithmetic and kernel entry declarations of libmlafold.
+// Host and device code of the library include this; nothing outside it does.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/mlafold.h"
+
+namespace mlafold {
+
+constexpr int kPage = 64;          // tokens per cache page
+constexpr int kDqk = 576;          // latent 512 + rope 64 (bytes per FP8 row)
+constexpr int kDv = 512;           // value = latent slice
+constexpr int kSplitBits = 12;     // work item = request << 12 | split
+constexpr int kMaxR = 1024;        // the planner runs one CTA with one thread per request
+constexpr int kMaxM = 4096;
+
+__host__ __device__ inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// Query rows of one request are processed in row blocks of 32 (M <= 32) or 64.
+__host__ __device__ inline int row_block(int M) { return M <= 32 ? 32 : 64; }
+__host__ __device__ inline int row_blocks(int M) { return (M + row_block(M) - 1) / row_block(M); }
+// Concurrent work items the plan targets.
+__host__ __device__ inline int plan_units(int M, int num_ctas) {
+  int u = num_ctas / row_blocks(M);
+  return u < 1 ? 1 : u;
+}
+__host__ __device__ inline int uniform_splits(int R, int M, int num_ctas, int max_splits) {
+  long long s = cdiv(plan_units(M, num_ctas), R > 0 ? R : 1);
+  if (s < 1) s = 1;
+  return (int)(s < max_splits ? s : max_splits);
+}
+inline int plan_list_len(const mla_shape& s) {
+  if (s.policy == MLA_POLICY_BALANCED) return plan_units(s.k * s.H, s.num_ctas) + s.R;
+  return s.R * uniform_splits(s.R, s.k * s.H, s.num_ctas, s.max_splits);
+}
+// Bound on items of multi-split requests; they occupy work-list slots [0, slots).
+inline int partial_slots(const mla_shape& s) {
+  int M = s.k * s.H;
+  if (s.policy == MLA_POLICY_BALANCED) {
+    int a = plan_list_len(s), b = 2 * plan_units(M, s.num_ctas);
+    return a < b ? a : b;
+  }
+  int u = uniform_splits(s.R, M, s.num_ctas, s.max_splits);
+  return u >= 2 ? s.R * u : 0;
+}
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// Workspace: FP32 partial outputs [slots][M][512], then FP32 LSEs [slots][M].
+inline size_t partial_out_bytes(int slots, int M) { return align256(size_t(slots) * M * kDv * 4); }
+inline size_t workspace_bytes(const mla_shape& s) {
+  int slots = partial_slots(s), M = s.k * s.H;
+  if (slots == 0) return 0;
+  return partial_out_bytes(slots, M) + align256(size_t(slots) * M * 4);
+}
+
+// Keys [j0, j1) of split s of n of a request of L keys (page-aligned cuts).
+__host__ __device__ inline void split_range(int L, int n, int s, int& j0, int& j1) {
+  long long p = cdiv(L, kPage);
+  long long p0 = (s * p) / n, p1 = ((s + 1) * p) / n;
+  j0 = (int)(kPage * p0);
+  long long e = kPage * p1;
+  j1 = (int)(e < L ? e : L);
+}
+
+struct DecodeArgs {
+  const uint8_t* q;
+  const uint8_t* kv;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* counts;
+  const int32_t* work;
+  float* part_o;     // [slots][M][512]
+  float* part_lse;   // [slots][M]
+  uint16_t* out;     // [R][M][512] bf16 bits
+  float* lse;        // [R][M]
+  int32_t* status;   // may be null
+  float bmm1_log2;   // bmm1_scale * log2(e)
+  float bmm2;
+  int R, M, max_pages, num_pages, list_len, slots;
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_plan(const mla_shape& s, const int32_t* seq_lens, int32_t* counts,
+                        int32_t* work, int list_len, cudaStream_t st);
+cudaError_t launch_combine(const mla_shape& s, const int32_t* counts, const int32_t* work,
+                           int list_len, const float* part_o, const float* part_lse, int slots,
+                           float bmm2, uint16_t* out, float* lse, cudaStream_t st);
+cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace mlafold

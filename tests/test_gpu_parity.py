@@ -1,0 +1,206 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import mla_decode_attention_folded_gb300 as mla
+import oracle.attention as att
+from oracle import planner as pl
+from tests.gpu_util import assert_close, oracle_full, run_decode, to_device, bmm_scales
+from workloads import WORKLOADS, make_batch, make_batch_from_lengths
+
+pytestmark = pytest.mark.gpu
+
+TINY = "R2_k4_H8_len100+37"
+FULL = [n for n in WORKLOADS if n != TINY]
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+# ---------------------------------------------------------------- planner
+def _gpu_plan(lens, M, G, mst, ms, policy):
+    R = len(lens)
+    s = mla.make_shape(R, 1, M, 1, 1, G, mst, ms, policy)
+    n = mla.plan_list_len(s)
+    d = torch.tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    counts = torch.zeros(R, dtype=torch.int32, device="cuda")
+    work = torch.full((n,), 7, dtype=torch.int32, device="cuda")   # not pre-filled with -1
+    mla.plan_splits(s, d, counts, work)
+    return counts.cpu().numpy(), work.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+@pytest.mark.parametrize("policy", [pl.BALANCED, pl.UNIFORM])
+def test_planner_bit_exact_on_workloads(name, policy):
+    w = WORKLOADS[name]
+    b = make_batch(name) if name == TINY else None
+    from workloads import draw_lengths
+    gen = torch.Generator().manual_seed(w.seed)
+    lens = draw_lengths(w.lengths, w.R, gen) if b is None else b.seq_lens.numpy()
+    for G in (8, _sms()):
+        c, wk = _gpu_plan(lens, w.M, G, 256, 64, policy)
+        c2, wk2 = pl.plan(lens, w.M, G, 256, 64, policy)
+        assert np.array_equal(c, c2) and np.array_equal(wk, wk2)
+
+
+def test_planner_bit_exact_random():
+    rng = np.random.default_rng(123)
+    for trial in range(2000):
+        R = int(rng.integers(1, 1025)) if trial % 50 == 0 else int(rng.integers(1, 200))
+        kind = trial % 4
+        if kind == 0:
+            lens = rng.integers(0, 9000, size=R)
+        elif kind == 1:
+            lens = np.clip(np.round(np.exp(rng.normal(7.6, 1.2, size=R))), 0, 200000).astype(int)
+        elif kind == 2:
+            lens = rng.integers(0, 3, size=R) * rng.integers(0, 200, size=R)
+        else:
+            lens = rng.integers(1, 600, size=R)
+            lens[0] = int(rng.integers(50000, 500000))
+        M = int(rng.choice([1, 8, 32, 33, 56, 64, 256, 448, 4096]))
+        G = int(rng.choice([1, 3, 148, 152, 304, 2048]))
+        mst = int(rng.choice([1, 64, 256, 5000]))
+        ms = int(rng.choice([1, 2, 64, 4096]))
+        policy = int(rng.integers(0, 2))
+        c, wk = _gpu_plan(lens, M, G, mst, ms, policy)
+        c2, wk2 = pl.plan(lens, M, G, mst, ms, policy)
+        assert np.array_equal(c, c2), (trial, R, M, G)
+        assert np.array_equal(wk, wk2), (trial, R, M, G)
+
+
+# ---------------------------------------------------------------- decode
+@pytest.mark.parametrize("policy", [pl.BALANCED, pl.UNIFORM])
+@pytest.mark.parametrize("num_ctas", [1, 8, None])
+def test_tiny_workload_matches_oracle(policy, num_ctas):
+    b = make_batch(TINY)
+    ref_o, ref_l = oracle_full(b)
+    out, lse, status, _ = run_decode(b, policy=policy, num_ctas=num_ctas, min_split_tokens=64)
+    assert status == 0
+    assert_close(out, lse, ref_o, ref_l, f"tiny policy={policy} ctas={num_ctas}")
+
+
+CASES = [
+    # lengths, k, H: ragged tails, page boundaries, empty and one-key requests
+    ((1, 63, 64, 65, 127, 128, 129), 2, 4),
+    ((0, 5, 0), 3, 2),
+    ((700, 1500, 3), 1, 1),
+    ((1000, 257, 4096), 4, 8),
+    ((333, 2000), 7, 8),
+    ((2100, 640), 3, 11),
+    ((1500,), 1, 64),
+    ((900, 130), 2, 40),
+    ((2500, 64), 4, 64),
+]
+
+
+@pytest.mark.parametrize("lens,k,H", CASES)
+@pytest.mark.parametrize("policy", [pl.BALANCED, pl.UNIFORM])
+def test_small_cases_match_oracle(lens, k, H, policy):
+    b = make_batch_from_lengths(lens, k, H, seed=sum(lens) + 17 * k + H, value_std=1.0,
+                                scaling="amax", fill=-5, extra_pages=3)
+    ref_o, ref_l = oracle_full(b)
+    for G in (2, 13, None):
+        out, lse, status, _ = run_decode(b, policy=policy, num_ctas=G, min_split_tokens=64)
+        assert status == 0
+        assert_close(out, lse, ref_o, ref_l, f"{lens} k={k} H={H} G={G}")
+    if max(lens) > 0:
+        empty = [i for i, L in enumerate(lens) if L == 0]
+        for i in empty:
+            assert torch.all(out[i] == 0) and torch.all(torch.isneginf(lse[i]))
+
+
+def test_folded_equals_unfolded():
+    b = make_batch_from_lengths((900, 77, 2000), 4, 8, seed=5, scaling="amax")
+    ref_o, ref_l = oracle_full(b)
+    for policy in (pl.BALANCED, pl.UNIFORM):
+        fo, fl, s1, _ = run_decode(b, policy=policy)
+        uo, ul, s2, _ = run_decode(b, policy=policy, folded=False)
+        assert s1 == 0 and s2 == 0
+        assert_close(fo, fl, ref_o, ref_l, "folded")
+        assert_close(uo, ul, ref_o, ref_l, "unfolded")
+
+
+def test_many_splits_of_one_request():
+    b = make_batch_from_lengths((20000,), 2, 16, seed=9, scaling="amax")
+    ref_o, ref_l = oracle_full(b)
+    out, lse, status, (counts, _) = run_decode(b, min_split_tokens=64, max_splits=4096)
+    assert status == 0 and int(counts[0]) > 100
+    assert_close(out, lse, ref_o, ref_l, "many splits")
+
+
+def test_out_of_range_page_sets_status_without_fault():
+    b = make_batch_from_lengths((300, 100), 2, 8, seed=3, scaling="amax")
+    b.block_table[0, 2] = b.kv.shape[0] + 1000          # inside request 0's pages
+    _, _, status, _ = run_decode(b)
+    assert status & mla.FAULT_PAGE_RANGE
+    b.block_table[0, 2] = -3
+    _, _, status, _ = run_decode(b)
+    assert status & mla.FAULT_PAGE_RANGE
+
+
+# ---------------------------------------------------------------- combine alone
+def test_combine_on_oracle_partials():
+    """mla_split_combine on partials the oracle made over the planned splits."""
+    b = make_batch_from_lengths((3000, 700, 64, 0), 2, 8, seed=77, scaling="amax")
+    G = 16
+    s = mla.make_shape(b.R, b.k, b.H, b.block_table.shape[1], b.kv.shape[0], G, 64, 64)
+    counts, work = pl.plan(b.seq_lens.numpy(), b.M, G, 64, 64, pl.BALANCED)
+    slots = pl.partial_slots(b.R, b.M, G, pl.BALANCED, 64)
+    ws = torch.zeros(mla.workspace_bytes(s), dtype=torch.uint8)
+    po_bytes = (slots * b.M * 512 * 4 + 255) // 256 * 256
+    po = ws[:po_bytes].view(torch.float32)[: slots * b.M * 512].view(slots, b.M, 512)
+    plse = ws[po_bytes:].view(torch.float32)[: slots * b.M].view(slots, b.M)
+    lens = b.seq_lens.numpy()
+    for idx, e in enumerate(work):
+        if e < 0:
+            break
+        r, sp = int(e) >> 12, int(e) & 4095
+        if counts[r] < 2:
+            continue
+        kr = np.zeros((b.R, 2), dtype=np.int64)
+        kr[r] = pl.split_range(int(lens[r]), int(counts[r]), sp)
+        o, l = att.mla_decode(b.q.numpy(), b.kv.numpy(), b.block_table.numpy(), lens, b.k,
+                              b.sm_scale, b.q_scale, b.kv_scale, key_range=kr, requests=[r])
+        po[idx] = torch.from_numpy(o.reshape(b.R, b.M, 512)[r] / b.kv_scale).float()
+        plse[idx] = torch.from_numpy(l.reshape(b.R, b.M)[r]).float()
+    out = torch.zeros((b.R, b.M, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((b.R, b.M), dtype=torch.float32, device="cuda")
+    mla.split_combine(s, torch.from_numpy(counts).cuda(), torch.from_numpy(work).cuda(),
+                      ws.cuda(), b.kv_scale, out, lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle_full(b)
+    multi = [r for r in range(b.R) if counts[r] >= 2]
+    assert multi
+    assert_close(out.float().cpu()[multi], lse.cpu()[multi], ref_o[multi], ref_l[multi],
+                 "combine")
+
+
+# ---------------------------------------------------------------- full sizes, sampled
+def _picks(b, counts, n=40, seed=0):
+    rng = np.random.default_rng(seed)
+    lens = b.seq_lens.numpy()
+    reqs = [int(np.argmax(lens)), int(np.argmin(lens))]
+    reqs += [int(r) for r in np.nonzero(counts.numpy() >= 2)[0][:3]]
+    reqs += [int(r) for r in rng.integers(0, b.R, size=4)]
+    picks = []
+    for r in dict.fromkeys(reqs):
+        for m in sorted(set([0, b.M - 1] + rng.integers(0, b.M, size=3).tolist())):
+            picks.append((r, m))
+    return picks[:n]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled(name):
+    b = make_batch(name)
+    out, lse, status, (counts, _) = run_decode(b)
+    assert status == 0
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    picks = _picks(b, counts)
+    ref_o, ref_l = att.mla_decode_rows(b.q.numpy(), b.kv.numpy(), b.block_table.numpy(),
+                                       b.seq_lens.numpy(), b.k, b.sm_scale, b.q_scale,
+                                       b.kv_scale, picks)
+    got_o = np.stack([out[r, m].numpy() for r, m in picks])
+    got_l = np.array([float(lse[r, m]) for r, m in picks])
+    assert_close(got_o, got_l, ref_o, ref_l, name)
