@@ -28,24 +28,44 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
                float* __restrict__ lse) {
   __shared__ int s_req[kMaxStarts];
   __shared__ int s_start[kMaxStarts];
+  __shared__ int s_warp[kWarps];
   __shared__ int s_nreq;
   grid_dep_wait();
+  // Ordered compaction of the multi-split requests' first items: every CTA
+  // must see the same list, in work-list order, to agree on row ownership.
+  const int lane = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_nreq = 0;
   __syncthreads();
   const int scan = min(list_len, slots);
-  for (int e = threadIdx.x; e < scan; e += blockDim.x) {
-    const int w = work[e];
-    if (w < 0 || (w & ((1 << kSplitBits) - 1)) != 0) continue;
-    const int r = w >> kSplitBits;
-    if (r >= R || counts[r] < 2) continue;
-    const int slot = atomicAdd(&s_nreq, 1);
-    if (slot < kMaxStarts) { s_req[slot] = r; s_start[slot] = e; }
+  for (int base = 0; base < scan; base += blockDim.x) {
+    const int e = base + threadIdx.x;
+    bool first = false;
+    int r = 0;
+    if (e < scan) {
+      const int w = work[e];
+      if (w >= 0 && (w & ((1 << kSplitBits) - 1)) == 0) {
+        r = w >> kSplitBits;
+        first = r < R && counts[r] >= 2;
+      }
+    }
+    const unsigned ballot = __ballot_sync(0xffffffffu, first);
+    if (lane == 0) s_warp[warp_id] = __popc(ballot);
+    __syncthreads();
+    int before = s_nreq;
+    for (int w = 0; w < warp_id; ++w) before += s_warp[w];
+    before += __popc(ballot & ((1u << lane) - 1u));
+    if (first && before < kMaxStarts) { s_req[before] = r; s_start[before] = e; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int add = 0;
+      for (int w = 0; w < kWarps; ++w) add += s_warp[w];
+      s_nreq += add;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   const int nreq = min(s_nreq, kMaxStarts);
   constexpr int kDims = kDv / BANDS;          // dims per warp
   constexpr int kVec = kDims / 32 / 4;        // float4 per lane
-  const int lane = threadIdx.x & 31;
   const long long total = (long long)nreq * M * BANDS;
   for (long long t = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); t < total;
        t += (long long)gridDim.x * kWarps) {
