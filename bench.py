@@ -38,13 +38,13 @@ METRIC = "decode rows/s and KV HBM GB/s (fraction of 8 TB/s) vs unfolded, 1 GB30
 UNIT = "rows/s"
 DEFAULT_WORKLOAD = "R32_k4_H8_len1k-8k"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ("decode_simt.cu", "decode_tc.cu", "internal.h", "ptx.cuh", "tc.cuh")
+DECODE_SOURCES = ("decode_tc.cu", "internal.h", "ptx.cuh", "tc.cuh")
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))

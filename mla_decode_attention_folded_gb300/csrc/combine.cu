@@ -31,6 +31,7 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
   __shared__ int s_warp[kWarps];
   __shared__ int s_nreq;
   grid_dep_wait();
+  grid_dep_launch();
   // Ordered compaction of the multi-split requests' first items: every CTA
   // must see the same list, in work-list order, to agree on row ownership.
   const int lane = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
@@ -76,28 +77,49 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
     const int r = s_req[qi], start = s_start[qi];
     const int n = counts[r];
     if (start + n > slots) continue;       // not a plan of this shape: nothing to read
-    // Max LSE over the splits (each lane strides the splits, then a warp max).
+    // Lanes hold 32 splits' LSEs at a time; the max, the weights and their sum
+    // come from shuffles, so only the partial rows are loaded per split.
+    const float* lrow = part_lse + (long long)start * M + m;
     float mx = -INFINITY;
-    for (int s = lane; s < n; s += 32) mx = fmaxf(mx, part_lse[(long long)(start + s) * M + m]);
+    for (int c0 = 0; c0 < n; c0 += 32)
+      if (c0 + lane < n) mx = fmaxf(mx, lrow[(long long)(c0 + lane) * M]);
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float z = 0.f;
     float4 acc[kVec];
 #pragma unroll
     for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float z = 0.f;
-    if (mx != -INFINITY) {
-      for (int s = 0; s < n; ++s) {
-        const long long row = (long long)(start + s) * M + m;
-        const float ls = part_lse[row];
-        const float w = ls == -INFINITY ? 0.f : ex2(ls - mx);
-        z += w;
-        const float4* src = reinterpret_cast<const float4*>(part_o + row * kDv + band * kDims);
+    const float* base = part_o + ((long long)start * M + m) * kDv + band * kDims;
+    const long long split_stride = (long long)M * kDv;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const float lc = c0 + lane < n ? lrow[(long long)(c0 + lane) * M] : -INFINITY;
+      const float wc = (mx == -INFINITY || lc == -INFINITY) ? 0.f : ex2(lc - mx);
+      z += wc;
+      const int cn = min(32, n - c0);
+      for (int s0 = 0; s0 < cn; s0 += 4) {
+        float4 o[4][kVec];
+        float w[4];
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) {
-          const float4 o = src[v * 32 + lane];
-          acc[v].x += w * o.x; acc[v].y += w * o.y; acc[v].z += w * o.z; acc[v].w += w * o.w;
+        for (int u = 0; u < 4; ++u) {          // four splits' loads in flight together
+          const int s = s0 + u;
+          w[u] = __shfl_sync(0xffffffffu, wc, s & 31);
+          const bool live = s < cn;
+          const float4* src =
+              reinterpret_cast<const float4*>(base + (live ? c0 + s : 0) * split_stride);
+#pragma unroll
+          for (int v = 0; v < kVec; ++v)
+            o[u][v] = live ? src[v * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!live) w[u] = 0.f;
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < kVec; ++v) {
+            acc[v].x += w[u] * o[u][v].x; acc[v].y += w[u] * o[u][v].y;
+            acc[v].z += w[u] * o[u][v].z; acc[v].w += w[u] * o[u][v].w;
+          }
       }
     }
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     const float scale = z > 0.f ? bmm2 / z : 0.f;
     uint16_t* dst = out + ((long long)r * M + m) * kDv + band * kDims;
 #pragma unroll
@@ -112,7 +134,6 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
     if (band == 0 && lane == 0)
       lse[(long long)r * M + m] = z > 0.f ? mx + __log2f(z) : -INFINITY;
   }
-  grid_dep_launch();
 }
 
 }  // namespace

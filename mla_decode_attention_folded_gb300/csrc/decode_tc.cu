@@ -1,0 +1,758 @@
+// Split-KV FP8 MLA decode on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// What it computes (drafter-attention page, module overview and
+// `folded_decode`; balanced-MLA page, module overview): for each work item of
+// the plan (request r, split s: keys [j0, j1)) and each block of NR query rows
+// of the request's M = k*H folded rows, the split's softmax attention over the
+// 576-dim latent keys with the 512-dim latent slice as the value, written as
+// BF16 out + base-2 LSE (one split) or as an FP32 partial + LSE (several).
+//
+// Design (ours; the pages' kernels are prior art only):
+// * Persistent CTAs, one per SM, walk the (item, row block) jobs round-robin.
+// * Swap-AB: keys are the MMA's M dimension (128 per tile = two pages) and
+//   query rows its N, so M = k*H of 32..448 needs no padding to 128 and the
+//   whole O^T accumulator (512 dims x N rows) plus two S^T buffers fit TMEM.
+//     S^T[128 keys, NR]  = K[128, 576] . Q[NR, 576]^T   (18 MMAs, K-major)
+//     O^T[512, NR(x2)]  += V^T[512, 128] . P^T[128, NR] (V = latent slice of
+//                          the same shared-memory tile, read MN-major)
+// * Warp roles: warp 0 issues TMA (per-page gathers through the block table
+//   into a 2-stage ring of 128-key tiles; Q block once per job); warp 1 issues
+//   the MMAs and owns TMEM; warps 2-5 (128 threads) own one key of the tile
+//   each for the softmax and one value dim per 128-dim band for the epilogue.
+// * Softmax in base 2 with a lazily updated row max: the max moves only when a
+//   new score exceeds it by more than 8 (P <= 2^8, balanced-MLA page, module
+//   overview). P enters the PV MMA as FP8 E4M3, unscaled, split into two E4M3
+//   terms hi = e4m3(p), lo = e4m3(p - hi) (both FP8 operands: one E4M3 term
+//   alone misses the +-(2e-2 + 2e-2|ref|) bound on short requests). The
+//   normaliser is the FP32 sum of p.
+// * Every mbarrier wait is bounded (2 s); on expiry the CTA sets
+//   MLA_FAULT_WAIT_TIMEOUT in the status word, stops, drains its own copies and
+//   MMAs, frees TMEM and returns. No trap, no unbounded spin.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace mlafold {
+namespace {
+
+constexpr int kTileKeys = 128;                    // keys per MMA tile (two pages)
+constexpr int kStages = 2;                        // KV tiles in flight
+constexpr int kThreads = 192;                     // 6 warps
+constexpr int kChunkBytes = kTileKeys * 128;      // one 128-dim latent band of a tile
+constexpr int kRopeBytes = kTileKeys * 64;        // the 64 rope dims of a tile
+constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;     // 73728
+constexpr int kPageBytes = kPage * kDqk;          // 36864 bytes per page
+constexpr int kOCols = 64;                        // TMEM columns per 128-dim band of O^T
+constexpr int kSCol0 = 4 * kOCols;                // S^T buffers start after O^T
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+template <int NR>
+struct Cfg {
+  static constexpr bool kHiloN = NR == 32;        // hi|lo side by side along N
+  static constexpr int kQChunk = NR * 128;
+  static constexpr int kQBytes = 4 * kQChunk + NR * 64;
+  static constexpr int kPBytes = kHiloN ? kTileKeys * 64 : 2 * kTileKeys * 64;
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffP = kOffQ + kQBytes;
+  static constexpr int kOffCtl = kOffP + 2 * kPBytes;
+  static constexpr uint32_t kIdescS = tc::idesc_e4m3_f32(128, NR, false, false);
+  static constexpr uint32_t kIdescPV = tc::idesc_e4m3_f32(128, 64, true, true);
+  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1 KB alignment");
+  static_assert(kSCol0 + 2 * NR <= (int)kTmemCols, "TMEM budget");
+};
+
+struct Ctl {
+  uint64_t kv_full[kStages];   // TMA -> MMA: tile landed
+  uint64_t pv_done[kStages];   // MMA -> TMA, softmax: PV of a tile finished (stage, P free)
+  uint64_t s_full[2];          // MMA -> softmax: S^T ready
+  uint64_t s_empty[2];         // softmax -> MMA: S^T read
+  uint64_t p_full[2];          // softmax -> MMA: P^T written, masked V rows zeroed
+  uint64_t q_full, q_empty;    // Q block of the job
+  uint64_t o_full, o_empty;    // O^T of the job
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  float m_run[64];             // running row max (base-2 scores)
+  float vec[64];               // rescale factors, then 1/l
+  float lse[64];
+  float red[4][64];            // cross-warp reduction scratch
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ctl,
+                                         int32_t* status) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = tc::globaltimer_ns();
+  while (true) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+    if (tc::globaltimer_ns() - t0 > kTimeoutNs) {
+      *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+      if (status) atomicOr(status, MLA_FAULT_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Reduce v[32] across the 32 lanes by halving exchanges (31 shuffles per
+// lane instead of 160); afterwards lane l holds the reduction of row l in v[0].
+template <int LEN, bool MAX>
+__device__ __forceinline__ void tr_step(float* v, int lane, int o) {
+  const bool upper = (lane & o) != 0;
+#pragma unroll
+  for (int i = 0; i < LEN / 2; ++i) {
+    const float send = upper ? v[i] : v[i + LEN / 2];
+    const float keep = upper ? v[i + LEN / 2] : v[i];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+    v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+  }
+}
+template <bool MAX>
+__device__ __forceinline__ void transpose_reduce32(float* v, int lane) {
+  tr_step<32, MAX>(v, lane, 16);
+  tr_step<16, MAX>(v, lane, 8);
+  tr_step<8, MAX>(v, lane, 4);
+  tr_step<4, MAX>(v, lane, 2);
+  tr_step<2, MAX>(v, lane, 1);
+}
+
+__device__ __forceinline__ void group_sync() {   // the 128 softmax threads
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+__device__ __forceinline__ bool group_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, 2, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+// Per-job facts every role derives identically from the plan.
+struct Job {
+  int r, blk, item, j0, j1, ntiles;
+  bool direct, skip;
+};
+
+__device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, bool report) {
+  Job jb;
+  jb.item = item;
+  jb.blk = blk;
+  jb.skip = false;
+  const int e = a.work[item];
+  const int r = e >> kSplitBits, s = e & ((1 << kSplitBits) - 1);
+  jb.r = r;
+  if (r >= a.R || s >= a.counts[r]) {
+    if (report && a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
+    jb.skip = true;
+    jb.j0 = jb.j1 = jb.ntiles = 0;
+    jb.direct = false;
+    return jb;
+  }
+  const int n = a.counts[r];
+  int L = max(a.seq_lens[r], 0);
+  if (L > a.max_pages * kPage) {          // never read past the block-table row
+    if (report && a.status) atomicOr(a.status, MLA_FAULT_PAGE_RANGE);
+    L = a.max_pages * kPage;
+  }
+  split_range(L, n, s, jb.j0, jb.j1);
+  jb.ntiles = (int)cdiv(jb.j1 - jb.j0, kTileKeys);
+  jb.direct = n == 1;
+  if (!jb.direct && item >= a.slots) {
+    if (report && a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
+    jb.skip = true;
+  }
+  return jb;
+}
+
+// ---------------------------------------------------------------- producer
+// Runs on all 32 lanes of warp 0: the lanes fetch the job's block-table
+// entries 32 at a time (lane i holds page i of the chunk, checked against the
+// cache), lane 0 waits on the ring and issues the TMA copies.
+template <int NR>
+__device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
+                         const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
+                         const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
+  using C = Cfg<NR>;
+  const int lane = threadIdx.x & 31;
+  uint32_t g = 0, x = 0;
+  int last_q_parity = -1;
+  int last_kv_parity[kStages] = {-1, -1};
+  const int njobs = a.list_len * nb;
+  bool ok = true;
+  auto wait0 = [&](uint64_t* bar, uint32_t parity) {
+    int r = 1;
+    if (lane == 0) r = wait_bar(bar, parity, ctl, a.status) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, r, 0) != 0;
+  };
+  auto fetch = [&](const Job& jb, int chunk) {   // page ids of job pages 32*chunk + lane
+    const int first = jb.j0 / kPage + chunk * 32 + lane;
+    const int end = (int)cdiv(jb.j1, kPage);
+    int p = -1;
+    if (first < end) {
+      p = a.block_table[(long long)jb.r * a.max_pages + first];
+      if (p < 0 || p >= a.num_pages) {
+        if (a.status) atomicOr(a.status, MLA_FAULT_PAGE_RANGE);
+        p = -1;
+      }
+    }
+    return p;
+  };
+  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
+    const int item = job / nb, blk = job % nb;
+    if (a.work[item] < 0) break;
+    const Job jb = read_job(a, item, blk, lane == 0);
+    if (jb.skip || jb.ntiles == 0) continue;
+    int cur = fetch(jb, 0), nxt = fetch(jb, 1);
+    if (x > 0 && !(ok = wait0(&ctl->q_empty, (x - 1) & 1))) break;
+    if (lane == 0) {
+      uint8_t* q = smem + C::kOffQ;
+      tc::mbar_arrive_expect_tx(&ctl->q_full, C::kQBytes);
+      for (int c = 0; c < 4; ++c)
+        tc::tma_load_3d(q + c * C::kQChunk, tm_q, &ctl->q_full, c * 128, blk * NR, jb.r);
+      tc::tma_load_3d(q + 4 * C::kQChunk, tm_qr, &ctl->q_full, 512, blk * NR, jb.r);
+    }
+    last_q_parity = x & 1;
+    for (int t = 0; t < jb.ntiles; ++t, ++g) {
+      if (t > 0 && (t & 15) == 0) {            // 16 tiles = 32 pages per chunk
+        cur = nxt;
+        nxt = fetch(jb, (t >> 4) + 1);
+      }
+      const int st = g & 1;
+      if (g >= 2 && !(ok = wait0(&ctl->pv_done[st], ((g >> 1) - 1) & 1))) break;
+      const int kbase = jb.j0 + t * kTileKeys;
+      const int pages = (kbase + kPage < jb.j1) ? 2 : 1;
+      const int pid0 = __shfl_sync(0xffffffffu, cur, (2 * t) & 31);
+      const int pid1 = __shfl_sync(0xffffffffu, cur, (2 * t + 1) & 31);
+      if (lane == 0) {
+        const int pid[2] = {pid0, pages == 2 ? pid1 : -1};
+        const int nvalid = (pid[0] >= 0) + (pid[1] >= 0);
+        uint8_t* stage = smem + st * kStageBytes;
+        tc::mbar_arrive_expect_tx(&ctl->kv_full[st], nvalid * kPageBytes);
+        for (int h = 0; h < 2; ++h) {
+          if (pid[h] < 0) continue;
+          const int row = pid[h] * kPage;
+          for (int c = 0; c < 4; ++c)
+            tc::tma_load_2d(stage + c * kChunkBytes + h * (kChunkBytes / 2), tm_kv,
+                            &ctl->kv_full[st], c * 128, row);
+          tc::tma_load_2d(stage + 4 * kChunkBytes + h * (kRopeBytes / 2), tm_kvr,
+                          &ctl->kv_full[st], 512, row);
+        }
+      }
+      last_kv_parity[st] = (g >> 1) & 1;
+    }
+    ++x;
+  }
+  // Never leave with copies in flight into this CTA's shared memory.
+  if (!ok && lane == 0) {
+    const unsigned long long t0 = tc::globaltimer_ns();
+    for (int st = 0; st < kStages; ++st)
+      while (last_kv_parity[st] >= 0 &&
+             !tc::mbar_try_wait(&ctl->kv_full[st], last_kv_parity[st]) &&
+             tc::globaltimer_ns() - t0 < kTimeoutNs) {
+      }
+    while (last_q_parity >= 0 && !tc::mbar_try_wait(&ctl->q_full, last_q_parity) &&
+           tc::globaltimer_ns() - t0 < kTimeoutNs) {
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+template <int NR>
+__device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_t tmem, int nb) {
+  using C = Cfg<NR>;
+  const uint32_t s_kv = tc::smem_u32(smem), s_q = tc::smem_u32(smem + C::kOffQ);
+  const uint32_t s_p = tc::smem_u32(smem + C::kOffP);
+  uint32_t g = 0, x = 0;
+  const int njobs = a.list_len * nb;
+  bool ok = true;
+
+  auto issue_s = [&](uint32_t gg) {
+    const int st = gg & 1;
+    const uint32_t d = tmem + kSCol0 + st * NR;
+    const uint32_t kv = s_kv + st * kStageBytes;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_e4m3(d, tc::smem_desc(kv + c * kChunkBytes + kk * 32, 16, 1024, tc::kSw128),
+                     tc::smem_desc(s_q + c * C::kQChunk + kk * 32, 16, 1024, tc::kSw128),
+                     C::kIdescS, (c | kk) != 0);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+      tc::mma_e4m3(d, tc::smem_desc(kv + 4 * kChunkBytes + kk * 32, 16, 512, tc::kSw64),
+                   tc::smem_desc(s_q + 4 * C::kQChunk + kk * 32, 16, 512, tc::kSw64),
+                   C::kIdescS, true);
+    tc::mma_commit(&ctl->s_full[st]);
+  };
+
+  auto issue_pv = [&](uint32_t gg, bool first) {
+    const int st = gg & 1;
+    const uint32_t kv = s_kv + st * kStageBytes;
+    const uint32_t p = s_p + st * C::kPBytes;
+#pragma unroll
+    for (int dt = 0; dt < 4; ++dt) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        // V^T band dt, keys 32kk..32kk+31: MN-major, 8-key groups 1 KB apart.
+        const uint64_t va = tc::smem_desc(kv + dt * kChunkBytes + kk * 32 * 128, kChunkBytes,
+                                          1024, tc::kSw128);
+        const bool acc = !(first && kk == 0);
+        if constexpr (C::kHiloN) {
+          tc::mma_e4m3(tmem + dt * kOCols, va,
+                       tc::smem_desc(p + kk * 32 * 64, kTileKeys * 64, 512, tc::kSw64),
+                       C::kIdescPV, acc);
+        } else {
+          tc::mma_e4m3(tmem + dt * kOCols, va,
+                       tc::smem_desc(p + kk * 32 * 64, kTileKeys * 64, 512, tc::kSw64),
+                       C::kIdescPV, acc);
+          tc::mma_e4m3(tmem + dt * kOCols, va,
+                       tc::smem_desc(p + kTileKeys * 64 + kk * 32 * 64, kTileKeys * 64, 512,
+                                     tc::kSw64),
+                       C::kIdescPV, true);
+        }
+      }
+    }
+    tc::mma_commit(&ctl->pv_done[st]);
+  };
+
+  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
+    const int item = job / nb, blk = job % nb;
+    if (a.work[item] < 0) break;
+    const Job jb = read_job(a, item, blk, false);
+    if (jb.skip || jb.ntiles == 0) continue;
+    if (!(ok = wait_bar(&ctl->q_full, x & 1, ctl, a.status))) break;
+    // Issue S(t) as soon as its tile landed and its S buffer is free, and PV(t)
+    // as soon as P(t) is written: neither waits on the other's inputs. S runs
+    // at most one tile ahead of PV (two S buffers).
+    int ns = 0, npv = 0;
+    unsigned long long t0 = 0;
+    while (npv < jb.ntiles) {
+      bool progress = false;
+      if (ns < jb.ntiles && ns <= npv + 1) {
+        const uint32_t gg = g + ns;
+        const int st = gg & 1;
+        if (tc::mbar_test_wait(&ctl->kv_full[st], (gg >> 1) & 1) &&
+            (gg < 2 || tc::mbar_test_wait(&ctl->s_empty[st], ((gg >> 1) - 1) & 1))) {
+          tc::fence_after_sync();
+          issue_s(gg);
+          if (ns == jb.ntiles - 1) tc::mma_commit(&ctl->q_empty);   // every S of the job issued
+          ++ns;
+          progress = true;
+        }
+      }
+      if (npv < ns) {
+        const uint32_t gg = g + npv;
+        const int st = gg & 1;
+        if (tc::mbar_test_wait(&ctl->p_full[st], (gg >> 1) & 1) &&
+            (npv > 0 || x == 0 || tc::mbar_test_wait(&ctl->o_empty, (x - 1) & 1))) {
+          tc::fence_after_sync();
+          issue_pv(gg, npv == 0);
+          ++npv;
+          progress = true;
+        }
+      }
+      if (progress) {
+        t0 = 0;
+      } else {
+        const unsigned long long now = tc::globaltimer_ns();
+        if (t0 == 0) t0 = now;
+        const bool expired = now - t0 > kTimeoutNs;
+        if (*reinterpret_cast<volatile int*>(&ctl->abort_flag) || expired) {
+          *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+          if (expired && a.status) atomicOr(a.status, MLA_FAULT_WAIT_TIMEOUT);
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (!ok) break;
+    tc::mma_commit(&ctl->o_full);
+    g += jb.ntiles;
+    ++x;
+  }
+  // Wait for every MMA this thread issued before TMEM is released.
+  tc::mma_commit(&ctl->drain);
+  const unsigned long long t0 = tc::globaltimer_ns();
+  while (!tc::mbar_try_wait(&ctl->drain, 0) && tc::globaltimer_ns() - t0 < kTimeoutNs) {
+  }
+}
+
+// ---------------------------------------------------------------- softmax + epilogue
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+  return r;
+}
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+template <int NR>
+__device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_t tmem,
+                                 int nb) {
+  using C = Cfg<NR>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;                   // TMEM lanes this warp may access
+  const int tl = quarter * 32 + lane;             // key of the tile / dim of a band
+  const int gt = threadIdx.x - 64;                // 0..127 within the group
+  const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+  uint32_t g = 0, x = 0;
+  const int njobs = a.list_len * nb;
+  bool ok = true;
+  float lp[NR];                                   // this key's share of each row sum
+
+  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
+    const int item = job / nb, blk = job % nb;
+    if (a.work[item] < 0) break;
+    const Job jb = read_job(a, item, blk, false);
+    if (jb.skip) continue;
+    const int m0 = blk * NR;
+    const int rows = min(NR, a.M - m0);
+    if (jb.ntiles == 0) {                          // empty split: out 0, lse -inf
+      for (int i = 0; i < rows; ++i)
+        for (int d = gt; d < kDv; d += 128) {
+          if (jb.direct)
+            a.out[((long long)jb.r * a.M + m0 + i) * kDv + d] = 0;
+          else
+            a.part_o[((long long)jb.item * a.M + m0 + i) * kDv + d] = 0.f;
+        }
+      if (gt < rows) {
+        if (jb.direct) a.lse[(long long)jb.r * a.M + m0 + gt] = -INFINITY;
+        else a.part_lse[(long long)jb.item * a.M + m0 + gt] = -INFINITY;
+      }
+      continue;
+    }
+    group_sync();                                  // previous job's readers are done
+    if (gt < NR) ctl->m_run[gt] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) lp[i] = 0.f;
+    group_sync();
+
+    for (int t = 0; t < jb.ntiles; ++t) {
+      const uint32_t gg = g + t;
+      const int st = gg & 1;
+      if (!(ok = wait_bar(&ctl->s_full[st], (gg >> 1) & 1, ctl, a.status))) break;
+      tc::fence_after_sync();
+      float xv[NR];
+      {
+        uint32_t raw[32];
+#pragma unroll
+        for (int h = 0; h < NR / 32; ++h) {
+          tc::tmem_ld32(tmem + lane_addr + kSCol0 + st * NR + h * 32, raw);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) xv[h * 32 + i] = __uint_as_float(raw[i]);
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&ctl->s_empty[st]);
+      const bool valid = jb.j0 + t * kTileKeys + tl < jb.j1;
+      bool exceed = false;
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        xv[i] = valid ? xv[i] * a.bmm1_log2 : -INFINITY;
+        exceed |= xv[i] > ctl->m_run[i] + 8.f;
+      }
+      if (group_any(exceed)) {
+        // Rows whose max grew by more than 8: take the tile max as the new max.
+#pragma unroll
+        for (int h = 0; h < NR / 32; ++h) {      // 32 rows at a time: fewer live registers
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = xv[h * 32 + i];
+          transpose_reduce32<true>(v, lane);
+          ctl->red[quarter][h * 32 + lane] = v[0];
+        }
+        group_sync();
+        if (gt < NR) {
+          const float tm = fmaxf(fmaxf(ctl->red[0][gt], ctl->red[1][gt]),
+                                 fmaxf(ctl->red[2][gt], ctl->red[3][gt]));
+          const float mo = ctl->m_run[gt];
+          const float mn = tm > mo + 8.f ? tm : mo;
+          ctl->vec[gt] = mo == -INFINITY ? 0.f : ex2(mo - mn);
+          ctl->m_run[gt] = mn;
+        }
+        group_sync();
+#pragma unroll
+        for (int i = 0; i < NR; ++i) lp[i] *= ctl->vec[i];
+        if (t > 0) {
+          // O^T holds tiles < gg: wait for the last PV, then scale its columns.
+          const uint32_t gp = gg - 1;
+          if (!(ok = wait_bar(&ctl->pv_done[gp & 1], (gp >> 1) & 1, ctl, a.status))) break;
+          tc::fence_after_sync();
+#pragma unroll
+          for (int dt = 0; dt < 4; ++dt) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t raw[32];
+              const uint32_t addr = tmem + lane_addr + dt * kOCols + h * 32;
+              tc::tmem_ld32(addr, raw);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float f = ctl->vec[C::kHiloN ? i : h * 32 + i];
+                raw[i] = __float_as_uint(__uint_as_float(raw[i]) * f);
+              }
+              tc::tmem_st32(addr, raw);
+            }
+          }
+          tc::tmem_wait_st();
+        }
+      }
+      // P buffer st is free once PV(gg - 2) finished.
+      if (gg >= 2 && !(ok = wait_bar(&ctl->pv_done[st], ((gg >> 1) - 1) & 1, ctl, a.status)))
+        break;
+      uint32_t hi[NR / 4], lo[NR / 4];
+#pragma unroll
+      for (int i = 0; i < NR; i += 4) {
+        float p[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          p[u] = ex2(xv[i + u] - ctl->m_run[i + u]);
+          lp[i + u] += p[u];
+        }
+        const uint32_t h01 = f32x2_to_f16x2(p[0], p[1]), h23 = f32x2_to_f16x2(p[2], p[3]);
+        const uint16_t e01 = f16x2_to_e4m3x2(h01), e23 = f16x2_to_e4m3x2(h23);
+        const uint16_t l01 = f16x2_to_e4m3x2(f16x2_sub(h01, e4m3x2_to_f16x2(e01)));
+        const uint16_t l23 = f16x2_to_e4m3x2(f16x2_sub(h23, e4m3x2_to_f16x2(e23)));
+        hi[i / 4] = (uint32_t)e01 | ((uint32_t)e23 << 16);
+        lo[i / 4] = (uint32_t)l01 | ((uint32_t)l23 << 16);
+      }
+      // P^T row of this key, MN-major with the 64-byte swizzle: 16-byte chunk c
+      // of key k lives at k*64 + ((c ^ ((k >> 1) & 3)) * 16).
+      uint8_t* pbuf = smem + C::kOffP + st * C::kPBytes;
+      const int sw = (tl >> 1) & 3;
+      if constexpr (C::kHiloN) {
+        uint4* row = reinterpret_cast<uint4*>(pbuf + tl * 64);
+        row[0 ^ sw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        row[1 ^ sw] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        row[2 ^ sw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        row[3 ^ sw] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+      } else {
+        uint4* rh = reinterpret_cast<uint4*>(pbuf + tl * 64);
+        uint4* rl = reinterpret_cast<uint4*>(pbuf + kTileKeys * 64 + tl * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          rh[c ^ sw] = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+          rl[c ^ sw] = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+        }
+      }
+      if (!valid) {                                // keys past the split: V rows must be 0
+        uint8_t* stage = smem + st * kStageBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4* vrow = reinterpret_cast<uint4*>(stage + c * kChunkBytes + tl * 128);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) vrow[u] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&ctl->p_full[st]);
+    }
+    if (!ok) break;
+
+    // Row sums across the 128 keys of every tile, then 1/l and the LSE.
+#pragma unroll
+    for (int h = 0; h < NR / 32; ++h) {
+      transpose_reduce32<false>(lp + h * 32, lane);
+      ctl->red[quarter][h * 32 + lane] = lp[h * 32];
+    }
+    group_sync();
+    if (gt < NR) {
+      const float l = ctl->red[0][gt] + ctl->red[1][gt] + ctl->red[2][gt] + ctl->red[3][gt];
+      ctl->vec[gt] = l > 0.f ? 1.f / l : 0.f;
+      ctl->lse[gt] = l > 0.f ? ctl->m_run[gt] + __log2f(l) : -INFINITY;
+    }
+    group_sync();
+    if (!(ok = wait_bar(&ctl->o_full, x & 1, ctl, a.status))) break;
+    tc::fence_after_sync();
+#pragma unroll 1
+    for (int dt = 0; dt < 4; ++dt) {
+      float o[NR];
+      {
+        uint32_t r0[32], r1[32];
+        tc::tmem_ld32(tmem + lane_addr + dt * kOCols, r0);
+        tc::tmem_ld32(tmem + lane_addr + dt * kOCols + 32, r1);
+        tc::tmem_wait_ld();
+        if constexpr (C::kHiloN) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            o[i] = __uint_as_float(r0[i]);
+            o[NR - 32 + i] = __uint_as_float(r1[i]);
+          }
+        }
+      }
+      const int d = dt * 128 + tl;
+      if (jb.direct) {
+        uint16_t* dst = a.out + ((long long)jb.r * a.M + m0) * kDv + d;
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+          if (i < rows) dst[(long long)i * kDv] = f32_to_bf16_bits(o[i] * ctl->vec[i] * a.bmm2);
+      } else {
+        float* dst = a.part_o + ((long long)jb.item * a.M + m0) * kDv + d;
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+          if (i < rows) dst[(long long)i * kDv] = o[i] * ctl->vec[i];
+      }
+    }
+    tc::fence_before_sync();
+    tc::mbar_arrive(&ctl->o_empty);
+    if (gt < rows) {
+      if (jb.direct) a.lse[(long long)jb.r * a.M + m0 + gt] = ctl->lse[gt];
+      else a.part_lse[(long long)jb.item * a.M + m0 + gt] = ctl->lse[gt];
+    }
+    g += jb.ntiles;
+    ++x;
+  }
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
+                 const __grid_constant__ CUtensorMap tm_kvr,
+                 const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_qr, int nb) {
+  using C = Cfg<NR>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::kOffCtl);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&ctl->kv_full[s], 1);
+      tc::mbar_init(&ctl->pv_done[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl->s_full[b], 1);
+      tc::mbar_init(&ctl->s_empty[b], 128);
+      tc::mbar_init(&ctl->p_full[b], 128);
+    }
+    tc::mbar_init(&ctl->q_full, 1);
+    tc::mbar_init(&ctl->q_empty, 1);
+    tc::mbar_init(&ctl->o_full, 1);
+    tc::mbar_init(&ctl->o_empty, 128);
+    tc::mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tm_kv);
+    tc::prefetch_tmap(&tm_kvr);
+    tc::prefetch_tmap(&tm_q);
+    tc::prefetch_tmap(&tm_qr);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  grid_dep_wait();      // the plan is complete; earlier readers of out/workspace are done
+  grid_dep_launch();    // the reducer may launch; it still waits for this grid to finish
+  if (warp == 0) {
+    producer<NR>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer<NR>(a, smem, ctl, tmem, nb);
+  } else {
+    softmax_epilogue<NR>(a, smem, ctl, tmem, nb);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NR>
+cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
+  using C = Cfg<NR>;
+  CUtensorMap tkv, tkvr, tq, tqr;
+  const cuuint64_t kv_dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)a.num_pages * kPage};
+  const cuuint64_t kv_str[1] = {(cuuint64_t)kDqk};
+  const cuuint32_t kv_box[2] = {128, kPage}, kvr_box[2] = {64, kPage};
+  const cuuint64_t q_dims[3] = {(cuuint64_t)kDqk, (cuuint64_t)a.M, (cuuint64_t)a.R};
+  const cuuint64_t q_str[2] = {(cuuint64_t)kDqk, (cuuint64_t)a.M * kDqk};
+  const cuuint32_t q_box[3] = {128, (cuuint32_t)NR, 1}, qr_box[3] = {64, (cuuint32_t)NR, 1};
+  if (!encode(&tkv, a.kv, 2, kv_dims, kv_str, kv_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode(&tkvr, a.kv, 2, kv_dims, kv_str, kvr_box, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode(&tq, a.q, 3, q_dims, q_str, q_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode(&tqr, a.q, 3, q_dims, q_str, qr_box, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  const int smem_bytes = C::kOffCtl + (int)sizeof(Ctl) + 1024;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int nb = row_blocks(a.M);
+  const long long jobs = (long long)a.list_len * nb;
+  const int grid = (int)(jobs < s.num_ctas ? jobs : s.num_ctas);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid > 0 ? grid : 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NR>, a, tkv, tkvr, tq, tqr, nb);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
+  return row_block(a.M) == 32 ? launch_nr<32>(s, a, st) : launch_nr<64>(s, a, st);
+}
+
+}  // namespace mlafold

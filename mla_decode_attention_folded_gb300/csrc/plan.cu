@@ -63,6 +63,7 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int R, int M, int num_ctas, in
   int L = live ? seq_lens[i] : 0;
   if (L < 0) L = 0;
   s_len[i] = live ? L : -1;               // dead slots rank after every request
+  grid_dep_launch();                      // the decode may start its prologue
   const int p = (int)cdiv(L, kPage);
 
   const long long T = block_sum<long long>((long long)p, s_red64);
@@ -139,7 +140,6 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int R, int M, int num_ctas, in
     counts[i] = n;
   }
   for (int e = total + i; e < list_len; e += blockDim.x) work[e] = -1;
-  grid_dep_launch();
 }
 
 }  // namespace
@@ -148,7 +148,7 @@ cudaError_t launch_plan(const mla_shape& s, const int32_t* seq_lens, int32_t* co
                         int32_t* work, int list_len, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3((unsigned)((s.R + 31) / 32 * 32));   // one thread per request
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
