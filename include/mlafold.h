@@ -63,7 +63,10 @@ typedef enum {
   MLA_ERR_LIST = -4,        /* list_len < mla_plan_list_len()                    */
   MLA_ERR_UNSUPPORTED = -5, /* page_size != 64, or the device is not sm_103      */
   MLA_ERR_CUDA = -6,        /* a CUDA runtime or driver call failed              */
-  MLA_ERR_ALIGN = -7        /* a pointer is not aligned as documented            */
+  MLA_ERR_ALIGN = -7,       /* a pointer is not aligned as documented            */
+  MLA_ERR_SCRATCH_LIMIT = -8 /* the shape needs more split-KV scratch than the
+                               library's fixed array holds (see
+                               mla_folded_decode_noalloc)                         */
 } mla_status;
 
 typedef enum {
@@ -154,6 +157,32 @@ int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
 int32_t mla_split_combine(const mla_shape *shape, const int32_t *counts, const int32_t *work,
                           int32_t list_len, const void *workspace, size_t workspace_bytes,
                           float bmm2_scale, void *out, float *lse, mla_stream_t stream);
+
+/* The decode of mla_folded_decode followed by mla_split_combine, for callers
+ * that cannot allocate device memory (a host application or plugin whose
+ * allocator owns the device, or code running while a memory pool is sized):
+ * instead of a caller workspace, the split-KV partials live in a fixed array
+ * of device memory that the library itself defines, MLA_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) per GPU, held from the moment the library's device code is loaded
+ * on that GPU until the process exits. The pages have no counterpart; it is
+ * an addition of this library.
+ *   Arguments, layouts and results are those of mla_folded_decode (which also
+ *   writes the multi-split rows here, as mla_split_combine would).
+ *   Returns MLA_ERR_SCRATCH_LIMIT, launching nothing, when
+ *   mla_workspace_bytes(shape) exceeds MLA_NOALLOC_SCRATCH_BYTES.
+ *   Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   The first call on a device looks the array's device address up
+ *   (cudaGetSymbolAddress) with that device current and caches it; make that
+ *   first call before any stream capture.
+ *   Every call on a device uses the same array: two calls whose work overlaps
+ *   on the GPU (different streams, no ordering between them) race and corrupt
+ *   each other's results. Nothing in the array needs clearing between calls. */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int32_t mla_folded_decode_noalloc(const mla_shape *shape, const void *q, const void *kv,
+                                  const int32_t *block_table, const int32_t *seq_lens,
+                                  float bmm1_scale, float bmm2_scale, const int32_t *counts,
+                                  const int32_t *work, int32_t list_len, void *out, float *lse,
+                                  int32_t *status, mla_stream_t stream);
 
 /* Bits the decode kernel ORs into *status. */
 #define MLA_FAULT_WAIT_TIMEOUT 0x1 /* a pipeline wait gave up; the CTA stopped early */

@@ -28,7 +28,7 @@ from ._lib import (FAULT_PAGE_RANGE, FAULT_WAIT_TIMEOUT, FAULT_WORK_ITEM, MlaErr
 
 __all__ = ["MlaShape", "MlaError", "POLICY_BALANCED", "POLICY_UNIFORM", "make_shape",
            "plan_list_len", "workspace_bytes", "plan_splits", "folded_decode",
-           "split_combine", "FoldedMla", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
+           "split_combine", "folded_decode_noalloc", "FoldedMla", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
            "FAULT_WORK_ITEM", "library_path"]
 
 PAGE = 64
@@ -90,6 +90,20 @@ def split_combine(shape: MlaShape, counts, work, workspace, bmm2_scale: float, o
     _lib.check("mla_split_combine", _lib.load().mla_split_combine(
         ctypes.byref(shape), _ptr(counts), _ptr(work), work.numel(), _ptr(workspace), ws_bytes,
         float(bmm2_scale), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def folded_decode_noalloc(shape: MlaShape, q, kv, block_table, seq_lens, bmm1_scale: float,
+                          bmm2_scale: float, counts, work, out, lse, status=None,
+                          stream=None) -> None:
+    """Decode plus LSE reduction with the library's own fixed device scratch
+    (no workspace argument, no allocation): for callers that may not allocate
+    device memory. Shapes whose workspace exceeds the library's 64 MiB scratch
+    raise MlaError(MLA_ERR_SCRATCH_LIMIT). Calls that overlap on the GPU share
+    that scratch and race."""
+    _lib.check("mla_folded_decode_noalloc", _lib.load().mla_folded_decode_noalloc(
+        ctypes.byref(shape), _ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens),
+        float(bmm1_scale), float(bmm2_scale), _ptr(counts), _ptr(work), work.numel(), _ptr(out),
+        _ptr(lse), _ptr(status), _stream(stream)))
 
 
 class FoldedMla:

@@ -14,13 +14,14 @@ LIB_PATH = os.path.join(HERE, "libmlafold.so")
 MLA_OK = 0
 STATUS_NAMES = {0: "MLA_OK", -1: "MLA_ERR_NULL", -2: "MLA_ERR_SHAPE", -3: "MLA_ERR_WORKSPACE",
                 -4: "MLA_ERR_LIST", -5: "MLA_ERR_UNSUPPORTED", -6: "MLA_ERR_CUDA",
-                -7: "MLA_ERR_ALIGN"}
+                -7: "MLA_ERR_ALIGN", -8: "MLA_ERR_SCRATCH_LIMIT"}
 POLICY_BALANCED, POLICY_UNIFORM = 0, 1
 FAULT_WAIT_TIMEOUT, FAULT_PAGE_RANGE, FAULT_WORK_ITEM = 0x1, 0x2, 0x4
 
 # Every symbol include/mlafold.h declares.
 EXPORTS = ("mla_plan_list_len", "mla_workspace_bytes", "mla_plan_splits",
-           "mla_folded_decode", "mla_split_combine")
+           "mla_folded_decode", "mla_split_combine", "mla_folded_decode_noalloc")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class MlaShape(ctypes.Structure):
@@ -60,6 +61,8 @@ def load() -> ctypes.CDLL:
     lib.mla_folded_decode.restype = I32
     lib.mla_split_combine.argtypes = [SP, P, P, I32, P, SZ, F, P, P, P]
     lib.mla_split_combine.restype = I32
+    lib.mla_folded_decode_noalloc.argtypes = [SP, P, P, P, P, F, F, P, P, I32, P, P, P, P]
+    lib.mla_folded_decode_noalloc.restype = I32
     _lib = lib
     return lib
 
