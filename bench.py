@@ -216,39 +216,95 @@ class Runner:
         self.bmm2 = float(batch.kv_scale)
         self.launches = 3 if self.mla.workspace_bytes(self.eng.shape) > 0 else 2
 
-    def step(self, ev=None):
+    def plan(self):
+        self.eng.plan(self.lens)
+
+    def decode(self):
         e = self.eng
-        e.plan(self.lens)
-        if ev is not None:
-            ev[0].record()
         self.mla.folded_decode(e.shape, self.q, self.kv, self.bt, self.lens, self.bmm1,
                                self.bmm2, e.counts, e.work, e.workspace, self.out, self.lse,
                                e.status)
-        if ev is not None:
-            ev[1].record()
+
+    def combine(self):
+        e = self.eng
         self.mla.split_combine(e.shape, e.counts, e.work, e.workspace, self.bmm2, self.out,
                                self.lse)
 
-    def timed(self, steps, warmup, flush, barrier=None):
-        for _ in range(warmup):
-            flush.zero_()
-            self.step()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    def step(self):
+        self.plan()
+        self.decode()
+        self.combine()
+
+    def graph(self, fn):
+        """fn's launches captured once into a CUDA graph (replayed per step, so
+        host launch overhead stays out of the timed region)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()                                  # warm: lazy set-up happens outside capture
+        torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        if barrier:
-            barrier()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            fn()
         torch.cuda.synchronize()
+        return g
+
+    def _time(self, g, steps, flush, before=None):
+        """Mean event time of replaying graph g over `steps` replays, L2
+        flushed (and `before` replayed) untimed ahead of each."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
         for i in range(steps):
-            flush.zero_()
+            flush()
+            if before is not None:
+                before.replay()
             ev[i][0].record()
-            self.step(ev=(ev[i][1], ev[i][2]))
-            ev[i][3].record()
+            g.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    def timed(self, steps, warmup, flush, barrier=None):
+        """Whole steps (plan + decode + combine, chained as a caller runs them)
+        timed one by one; returns the mean step time in ms."""
+        g = self.graph(self.step)
+        for _ in range(warmup):
+            flush()
+            g.replay()
         torch.cuda.synchronize()
         if barrier:
             barrier()
-        step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-        dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
-        return statistics.mean(step_ms), statistics.mean(dec_ms)
+        torch.cuda.synchronize()
+        ms = self._time(g, steps, flush)
+        if barrier:
+            barrier()
+        return ms
+
+    def kernel_times(self, steps, flush):
+        """Each kernel alone (its inputs prepared untimed): plan, decode, combine."""
+        gp, gd, gc = self.graph(self.plan), self.graph(self.decode), self.graph(self.combine)
+        gpd = self.graph(lambda: (self.plan(), self.decode()))
+        plan = self._time(gp, steps, flush)
+        dec = self._time(gd, steps, flush, before=gp)
+        comb = self._time(gc, steps, flush, before=gpd)
+        return plan, dec, comb
+
+
+class L2Flush:
+    """Evicts L2 before a timed step: write a buffer of twice the L2 size, then
+    read another one, so L2 holds neither the inputs nor dirty lines whose
+    write-back would land inside the timed region."""
+
+    def __init__(self, dev):
+        n = 2 * max(torch.cuda.get_device_properties(dev).L2_cache_size, 64 << 20)
+        self.w = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(n // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
 
 
 def e2e_rows_per_s(batch, dev, steps):
@@ -311,14 +367,14 @@ def run_ours(args):
 
     w = WORKLOADS[args.workload]
     batch = make_batch(args.workload)
-    props = torch.cuda.get_device_properties(dev)
-    flush = torch.empty(2 * max(props.L2_cache_size, 64 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     main = Runner(batch, dev, policy=0, folded=True)
     clocks = ClockSampler(local)
     clocks.start()
-    step_ms, dec_ms = main.timed(args.steps, max(args.warmup, 3), flush, barrier)
+    step_ms = main.timed(args.steps, max(args.warmup, 3), flush, barrier)
     clk = clocks.stop()
+    plan_ms, dec_ms, comb_ms = main.kernel_times(min(args.steps, 1000), flush)
     status = int(main.eng.status.item())
     if world > 1:
         import torch.distributed as dist
@@ -339,9 +395,9 @@ def run_ours(args):
         for name, policy, folded in (("folded_uniform", 1, True), ("unfolded_balanced", 0, False),
                                      ("unfolded_uniform", 1, False)):
             r = Runner(batch, dev, policy=policy, folded=folded)
-            ms, dms = r.timed(args.variant_steps, 5, flush)
+            ms = r.timed(args.variant_steps, 5, flush)
             variants[name] = {"rows_per_s": rows / (ms / 1e3), "ms_per_step": ms,
-                              "decode_ms": dms, "kv_gbs": kv_b / (ms / 1e3) / 1e9}
+                              "kv_gbs": kv_b / (ms / 1e3) / 1e9}
             del r
 
     e2e_v, h2d, d2h = e2e_rows_per_s(batch, dev, args.e2e_steps)
@@ -368,12 +424,12 @@ def run_ours(args):
         "config": {"workload": args.workload, "R": batch.R, "k": batch.k, "H": batch.H,
                    "M": batch.M, "policy": "balanced", "num_ctas": main.eng.shape.num_ctas,
                    "kv_tokens": int(lens.sum()), "accumulate": "f32",
-                   "l2": "flushed before every step (2x L2 write, untimed)",
+                   "l2": "flushed before every step (2x L2 write + 2x L2 read, untimed)", "timing": "CUDA graph per step, events around each replay",
                    "parallelism": f"replicas{world}"},
         "kv_gbs": kv_b / (step_ms / 1e3) / 1e9,
         "kv_frac_of_8tbs": kv_b / (step_ms / 1e3) / 8e12,
         "head_rows_per_s": world * batch.R * batch.M / (step_ms / 1e3),
-        "decode_ms": dec_ms,
+        "kernel_ms": {"plan": plan_ms, "decode": dec_ms, "combine": comb_ms},
         "variants": variants,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,

@@ -334,6 +334,18 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
     unsigned long long t0 = 0;
     while (npv < jb.ntiles) {
       bool progress = false;
+      // PV first: its completion frees a KV stage for the next TMA.
+      if (npv < ns) {
+        const uint32_t gg = g + npv;
+        const int st = gg & 1;
+        if (tc::mbar_test_wait(&ctl->p_full[st], (gg >> 1) & 1) &&
+            (npv > 0 || x == 0 || tc::mbar_test_wait(&ctl->o_empty, (x - 1) & 1))) {
+          tc::fence_after_sync();
+          issue_pv(gg, npv == 0);
+          ++npv;
+          progress = true;
+        }
+      }
       if (ns < jb.ntiles && ns <= npv + 1) {
         const uint32_t gg = g + ns;
         const int st = gg & 1;
@@ -343,17 +355,6 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
           issue_s(gg);
           if (ns == jb.ntiles - 1) tc::mma_commit(&ctl->q_empty);   // every S of the job issued
           ++ns;
-          progress = true;
-        }
-      }
-      if (npv < ns) {
-        const uint32_t gg = g + npv;
-        const int st = gg & 1;
-        if (tc::mbar_test_wait(&ctl->p_full[st], (gg >> 1) & 1) &&
-            (npv > 0 || x == 0 || tc::mbar_test_wait(&ctl->o_empty, (x - 1) & 1))) {
-          tc::fence_after_sync();
-          issue_pv(gg, npv == 0);
-          ++npv;
           progress = true;
         }
       }
@@ -579,6 +580,11 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     group_sync();
     if (!(ok = wait_bar(&ctl->o_full, x & 1, ctl, a.status))) break;
     tc::fence_after_sync();
+    // Each 128-dim band of O^T goes through the P buffers (idle now: the last
+    // PV has finished) so that global stores are 16-byte row vectors.
+    uint8_t* stage = smem + C::kOffP;
+    const int row_bytes = jb.direct ? 128 * 2 : 128 * 4;      // one band of one row
+    const int chunks = rows * (row_bytes / 16);
 #pragma unroll 1
     for (int dt = 0; dt < 4; ++dt) {
       float o[NR];
@@ -598,18 +604,27 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
           }
         }
       }
-      const int d = dt * 128 + tl;
       if (jb.direct) {
-        uint16_t* dst = a.out + ((long long)jb.r * a.M + m0) * kDv + d;
+        uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
 #pragma unroll
         for (int i = 0; i < NR; ++i)
-          if (i < rows) dst[(long long)i * kDv] = f32_to_bf16_bits(o[i] * ctl->vec[i] * a.bmm2);
+          st16[i * 128 + tl] = f32_to_bf16_bits(o[i] * ctl->vec[i] * a.bmm2);
       } else {
-        float* dst = a.part_o + ((long long)jb.item * a.M + m0) * kDv + d;
+        float* st32 = reinterpret_cast<float*>(stage);
 #pragma unroll
-        for (int i = 0; i < NR; ++i)
-          if (i < rows) dst[(long long)i * kDv] = o[i] * ctl->vec[i];
+        for (int i = 0; i < NR; ++i) st32[i * 128 + tl] = o[i] * ctl->vec[i];
       }
+      group_sync();
+      uint8_t* dst = jb.direct
+          ? reinterpret_cast<uint8_t*>(a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128)
+          : reinterpret_cast<uint8_t*>(a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128);
+      const long long pitch = jb.direct ? kDv * 2 : kDv * 4;
+      for (int c = gt; c < chunks; c += 128) {
+        const int row = c / (row_bytes / 16), col = c % (row_bytes / 16);
+        *reinterpret_cast<uint4*>(dst + row * pitch + col * 16) =
+            *reinterpret_cast<const uint4*>(stage + row * row_bytes + col * 16);
+      }
+      group_sync();
     }
     tc::fence_before_sync();
     tc::mbar_arrive(&ctl->o_empty);

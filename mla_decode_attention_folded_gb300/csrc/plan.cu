@@ -73,21 +73,24 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int R, int M, int num_ctas, in
 
   int n = 1;
   if (policy == MLA_POLICY_BALANCED) {
-    long long c = cdiv(T, U);
-    if (c < minp) c = minp;
-    auto count = [&](long long cc) {
-      int mine = p > 0 ? (int)min((long long)max_splits, cdiv(p, cc)) : 0;
+    long long c0 = cdiv(T, U);
+    if (c0 < minp) c0 = minp;
+    // A chunk above the longest request gives every request one split, as the
+    // longest request's own length does: clamp so 32-bit division suffices.
+    int c = (int)(c0 < maxp ? c0 : (maxp > 0 ? maxp : 1));
+    auto count = [&](int cc) {
+      int mine = p > 0 ? min(max_splits, (p + cc - 1) / cc) : 0;
       return block_sum<int>(mine, s_red);
     };
     if (Rn <= U && count(c) > U) {        // block-uniform branch
-      long long lo = c + 1, hi = maxp;    // count(maxp) = Rn <= U
+      int lo = c + 1, hi = maxp;          // count(maxp) = Rn <= U
       while (lo < hi) {
-        long long mid = (lo + hi) / 2;
+        const int mid = (lo + hi) / 2;
         if (count(mid) <= U) hi = mid; else lo = mid + 1;
       }
       c = lo;
     }
-    n = p > 0 ? (int)min((long long)max_splits, cdiv(p, c)) : 1;
+    n = p > 0 ? min(max_splits, (p + c - 1) / c) : 1;
   } else {
     const int S = uniform_splits(R, M, num_ctas, max_splits);
     n = L > 0 ? min(S, p) : 1;
