@@ -290,6 +290,15 @@ class Runner:
         comb = self._time(gc, steps, flush, before=gpd)
         return plan, dec, comb
 
+    def marginal_times(self, steps, flush):
+        """Chained step time without the plan, and without the combine: how
+        much each adds to the chain (PDL overlap included)."""
+        g_no_comb = self.graph(lambda: (self.plan(), self.decode()))
+        g_no_plan = self.graph(lambda: (self.decode(), self.combine()))
+        gp = self.graph(self.plan)
+        return (self._time(g_no_plan, steps, flush, before=gp),
+                self._time(g_no_comb, steps, flush))
+
 
 class L2Flush:
     """Evicts L2 before a timed step: write a buffer of twice the L2 size, then
@@ -375,6 +384,7 @@ def run_ours(args):
     step_ms = main.timed(args.steps, max(args.warmup, 3), flush, barrier)
     clk = clocks.stop()
     plan_ms, dec_ms, comb_ms = main.kernel_times(min(args.steps, 1000), flush)
+    no_plan_ms, no_comb_ms = main.marginal_times(min(args.steps, 1000), flush)
     status = int(main.eng.status.item())
     if world > 1:
         import torch.distributed as dist
@@ -430,6 +440,7 @@ def run_ours(args):
         "kv_frac_of_8tbs": kv_b / (step_ms / 1e3) / 8e12,
         "head_rows_per_s": world * batch.R * batch.M / (step_ms / 1e3),
         "kernel_ms": {"plan": plan_ms, "decode": dec_ms, "combine": comb_ms},
+        "chain_ms": {"step": step_ms, "without_plan": no_plan_ms, "without_combine": no_comb_ms},
         "variants": variants,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,

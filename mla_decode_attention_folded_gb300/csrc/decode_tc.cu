@@ -401,6 +401,26 @@ __device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Copy one staged 128-dim band of `rows` rows (BF16 out or FP32 partial) to
+// global memory as 16-byte row vectors; the 128 group threads stride the
+// chunks, fully unrolled so the loads pipeline.
+template <int NR, bool DIRECT>
+__device__ __forceinline__ void copy_band(const uint8_t* stage, uint8_t* dst, int rows, int gt) {
+  constexpr int kRowBytes = DIRECT ? 128 * 2 : 128 * 4;
+  constexpr int kCpr = kRowBytes / 16;               // 16-byte chunks per row
+  constexpr long long kPitch = DIRECT ? kDv * 2 : kDv * 4;
+  constexpr int kIters = NR * kCpr / 128;
+  uint4 v[kIters];
+#pragma unroll
+  for (int it = 0; it < kIters; ++it)
+    v[it] = *reinterpret_cast<const uint4*>(stage + (it * 128 + gt) * 16);
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int c = it * 128 + gt, row = c / kCpr, col = c % kCpr;
+    if (row < rows) *reinterpret_cast<uint4*>(dst + row * kPitch + col * 16) = v[it];
+  }
+}
+
 template <int NR>
 __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_t tmem,
                                  int nb) {
@@ -583,8 +603,9 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     // Each 128-dim band of O^T goes through the P buffers (idle now: the last
     // PV has finished) so that global stores are 16-byte row vectors.
     uint8_t* stage = smem + C::kOffP;
-    const int row_bytes = jb.direct ? 128 * 2 : 128 * 4;      // one band of one row
-    const int chunks = rows * (row_bytes / 16);
+    float sc[NR];                                  // per-row output scale
+#pragma unroll
+    for (int i = 0; i < NR; ++i) sc[i] = ctl->vec[i] * (jb.direct ? a.bmm2 : 1.f);
 #pragma unroll 1
     for (int dt = 0; dt < 4; ++dt) {
       float o[NR];
@@ -608,22 +629,21 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
         uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
 #pragma unroll
         for (int i = 0; i < NR; ++i)
-          st16[i * 128 + tl] = f32_to_bf16_bits(o[i] * ctl->vec[i] * a.bmm2);
+          st16[i * 128 + tl] = f32_to_bf16_bits(o[i] * sc[i]);
       } else {
         float* st32 = reinterpret_cast<float*>(stage);
 #pragma unroll
-        for (int i = 0; i < NR; ++i) st32[i * 128 + tl] = o[i] * ctl->vec[i];
+        for (int i = 0; i < NR; ++i) st32[i * 128 + tl] = o[i] * sc[i];
       }
       group_sync();
-      uint8_t* dst = jb.direct
-          ? reinterpret_cast<uint8_t*>(a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128)
-          : reinterpret_cast<uint8_t*>(a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128);
-      const long long pitch = jb.direct ? kDv * 2 : kDv * 4;
-      for (int c = gt; c < chunks; c += 128) {
-        const int row = c / (row_bytes / 16), col = c % (row_bytes / 16);
-        *reinterpret_cast<uint4*>(dst + row * pitch + col * 16) =
-            *reinterpret_cast<const uint4*>(stage + row * row_bytes + col * 16);
-      }
+      if (jb.direct)
+        copy_band<NR, true>(stage, reinterpret_cast<uint8_t*>(
+                                       a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128),
+                            rows, gt);
+      else
+        copy_band<NR, false>(stage, reinterpret_cast<uint8_t*>(
+                                        a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128),
+                             rows, gt);
       group_sync();
     }
     tc::fence_before_sync();

@@ -27,6 +27,7 @@ constexpr int kThreads = kMaxR;   // one thread per request
 template <typename T>
 __device__ T block_sum(T v, T* red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (blockDim.x == 32) return v;        // one warp: no shared-memory round trip
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __syncthreads();                       // red[] may still be read by a previous call
   if (lane == 0) red[warp] = v;
@@ -38,6 +39,7 @@ __device__ T block_sum(T v, T* red) {
 
 __device__ int block_max(int v, int* red) {
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (blockDim.x == 32) return v;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __syncthreads();
   if (lane == 0) red[warp] = v;
