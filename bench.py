@@ -181,6 +181,17 @@ def profiled_traffic(workload: str):
         return None
 
 
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank values over the process group (identity
+    without one): the slowest rank's time sets a multi-rank result."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -197,18 +208,17 @@ class Runner:
         import mla_decode_attention_folded_gb300 as mla
         self.mla = mla
         self.b = batch
-        if folded:
-            R, k, H = batch.R, batch.k, batch.H
-            bt, lens = batch.block_table, batch.seq_lens
-        else:
-            rep = torch.arange(batch.R).repeat_interleave(batch.k)
-            R, k, H = batch.R * batch.k, 1, batch.H
-            bt, lens = batch.block_table[rep].contiguous(), batch.seq_lens[rep].contiguous()
+        # Unfolded = the stock layout: k single-token row groups per request,
+        # each reading the request's KV on its own.
+        R, k, H = batch.R, batch.k, batch.H
+        groups = 1 if folded else batch.k
+        bt, lens = batch.block_table, batch.seq_lens
         self.q = batch.q.to(dev)
         self.kv = batch.kv.to(dev)
         self.bt = bt.to(dev)
         self.lens = lens.to(dev)
-        self.eng = mla.FoldedMla(R, k, H, self.bt.shape[1], self.kv.shape[0], dev, policy=policy)
+        self.eng = mla.FoldedMla(R, k, H, self.bt.shape[1], self.kv.shape[0], dev, policy=policy,
+                                 groups=groups)
         self.out = torch.empty((R, k * H, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((R, k * H), dtype=torch.float32, device=dev)
         self.bmm1 = float(np.float32(batch.sm_scale) * np.float32(batch.q_scale)
@@ -386,11 +396,7 @@ def run_ours(args):
     plan_ms, dec_ms, comb_ms = main.kernel_times(min(args.steps, 1000), flush)
     no_plan_ms, no_comb_ms = main.marginal_times(min(args.steps, 1000), flush)
     status = int(main.eng.status.item())
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_ms, dec_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, dec_ms = float(t[0]), float(t[1])
+    step_ms, dec_ms = max_over_ranks([step_ms, dec_ms], dev)
 
     lens = batch.seq_lens.numpy()
     rows = batch.R * batch.k

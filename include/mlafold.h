@@ -81,7 +81,7 @@ typedef enum {
 
 /* Problem shape and plan parameters. All fields are host values. */
 typedef struct {
-  int32_t R;                /* requests in the batch, 1..1024                              */
+  int32_t R;                /* requests in the batch (distinct KV), >= 1                   */
   int32_t k;                /* query tokens per request (draft block), >= 1                */
   int32_t H;                /* heads per token, >= 1; M = k*H rows per request, <= 4096    */
   int32_t page_size;        /* tokens per cache page; must be 64                           */
@@ -92,6 +92,13 @@ typedef struct {
   int32_t min_split_tokens; /* smallest split a long request is cut into, >= 1 (e.g. 256)  */
   int32_t max_splits;       /* largest split count of one request, 1..4096 (e.g. 64)       */
   int32_t policy;           /* mla_policy                                                   */
+  int32_t groups;           /* row groups per request, dividing k (0 is read as 1): the k
+                               tokens of a request form `groups` decode rows of k/groups
+                               tokens x H heads that all read the request's one KV (its
+                               block_table row and seq_lens entry). 1 = full fold; k = the
+                               stock unfolded layout; in between = the partial fold of the
+                               drafter-attention page's `fold_plan`. Memory layouts of q,
+                               out and lse do not change. R * groups <= 1024.              */
 } mla_shape;
 
 /* Capacity, in entries, of the work list `work` that mla_plan_splits fills
@@ -109,10 +116,11 @@ int32_t mla_workspace_bytes(const mla_shape *shape, size_t *bytes);
 
 /* Plan the step's splits on the device (one CTA), from the KV lengths.
  *   seq_lens [R] int32, device: keys per request (negative is read as 0).
- *   counts   [R] int32, device, written: splits of each request (>= 1).
- *   work     [list_len] int32, device, written: items (request << 12 | split),
- *            requests longest first (ties: lower index first), splits in
- *            ascending order, then -1 to the end.
+ *   counts   [R*groups] int32, device, written: splits of each decode row group (>= 1).
+ *   work     [list_len] int32, device, written: items (row group << 12 | split),
+ *            row groups longest first (ties: lower index first), splits in
+ *            ascending order, then -1 to the end. Row group g reads request
+ *            g / groups.
  *   list_len must be >= mla_plan_list_len(shape).
  * Integer arithmetic only; the result is a pure function of the lengths and
  * the shape (the project's CPU planner reproduces it bit for bit). */
@@ -157,6 +165,19 @@ int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
 int32_t mla_split_combine(const mla_shape *shape, const int32_t *counts, const int32_t *work,
                           int32_t list_len, const void *workspace, size_t workspace_bytes,
                           float bmm2_scale, void *out, float *lse, mla_stream_t stream);
+
+/* Merge of S partial results of the same rows over disjoint key sets, e.g.
+ * the S shards of a decode-context-parallel KV cache each decoded on its own
+ * (drafter-attention page, `DraftDcp`: each head's rows are merged over the
+ * DCP sources by exp2(lse - max) / sum in FP32 with one BF16 rounding):
+ *   w_s = 2^(lse_s - max_s lse_s), out = sum_s w_s out_s / sum_s w_s,
+ *   lse = max + log2 sum_s w_s; rows whose sources are all empty get 0, -inf.
+ *   parts_out [S, rows, 512] BF16, device, 16-byte aligned: each source's out.
+ *   parts_lse [S, rows] FP32 base-2 LSE, device.
+ *   out [rows, 512] BF16 (16-byte aligned), lse [rows] FP32, device, written.
+ * S in 1..4096, rows >= 1. Moving the sources between GPUs is the caller's. */
+int32_t mla_lse_merge(int32_t S, int32_t rows, const void *parts_out, const float *parts_lse,
+                      void *out, float *lse, mla_stream_t stream);
 
 /* The decode of mla_folded_decode followed by mla_split_combine, for callers
  * that cannot allocate device memory (a host application or plugin whose

@@ -28,7 +28,7 @@ from ._lib import (FAULT_PAGE_RANGE, FAULT_WAIT_TIMEOUT, FAULT_WORK_ITEM, MlaErr
 
 __all__ = ["MlaShape", "MlaError", "POLICY_BALANCED", "POLICY_UNIFORM", "make_shape",
            "plan_list_len", "workspace_bytes", "plan_splits", "folded_decode",
-           "split_combine", "folded_decode_noalloc", "FoldedMla", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
+           "split_combine", "lse_merge", "folded_decode_noalloc", "FoldedMla", "fold_factor", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
            "FAULT_WORK_ITEM", "library_path"]
 
 PAGE = 64
@@ -52,9 +52,22 @@ def _stream(stream) -> int | None:
 
 def make_shape(R: int, k: int, H: int, max_pages: int, num_pages: int, num_ctas: int,
                min_split_tokens: int = 256, max_splits: int = 64,
-               policy: int = POLICY_BALANCED) -> MlaShape:
+               policy: int = POLICY_BALANCED, groups: int = 1) -> MlaShape:
     return MlaShape(R, k, H, PAGE, max_pages, num_pages, num_ctas, min_split_tokens,
-                    max_splits, policy)
+                    max_splits, policy, groups)
+
+
+def fold_factor(k: int, H: int, max_heads: int = 128) -> int:
+    """Tokens folded into one decode row when a row may hold at most
+    `max_heads` heads: the largest divisor f of k with f * H <= max_heads
+    (1 when even one token's heads exceed it). The drafter-attention page's
+    `fold_plan` rule for the LSE-returning kernel (its example: k = 4 at 64
+    heads folds pairs). Use groups = k // f row groups per request."""
+    best = 1
+    for f in range(1, k + 1):
+        if k % f == 0 and f * H <= max_heads:
+            best = f
+    return best
 
 
 def plan_list_len(shape: MlaShape) -> int:
@@ -92,6 +105,15 @@ def split_combine(shape: MlaShape, counts, work, workspace, bmm2_scale: float, o
         float(bmm2_scale), _ptr(out), _ptr(lse), _stream(stream)))
 
 
+def lse_merge(parts_out, parts_lse, out, lse, stream=None) -> None:
+    """Merge S partial results over disjoint key sets: parts_out [S, rows, 512]
+    BF16 and parts_lse [S, rows] FP32 log2 -> out [rows, 512], lse [rows]
+    (the decode-context-parallel combine; see include/mlafold.h)."""
+    S, rows = parts_lse.shape[0], parts_lse.numel() // parts_lse.shape[0]
+    _lib.check("mla_lse_merge", _lib.load().mla_lse_merge(
+        S, rows, _ptr(parts_out), _ptr(parts_lse), _ptr(out), _ptr(lse), _stream(stream)))
+
+
 def folded_decode_noalloc(shape: MlaShape, q, kv, block_table, seq_lens, bmm1_scale: float,
                           bmm2_scale: float, counts, work, out, lse, status=None,
                           stream=None) -> None:
@@ -107,7 +129,10 @@ def folded_decode_noalloc(shape: MlaShape, q, kv, block_table, seq_lens, bmm1_sc
 
 
 class FoldedMla:
-    """Plan buffers and split-KV workspace of one decode shape.
+    """Plan buffers and split-KV workspace of one decode shape. `groups` row
+    groups per request (a divisor of k): 1 folds all k tokens into one decode
+    row, k is the stock unfolded layout, `k // fold_factor(k, H)` the partial
+    fold of the pages' `fold_plan`; out and lse keep the same layout.
 
     Everything is allocated here, before any capture; ``plan`` and ``decode``
     only launch kernels (balanced-MLA page, ``BalancedMla.require``: prepared
@@ -115,15 +140,16 @@ class FoldedMla:
 
     def __init__(self, R: int, k: int, H: int, max_pages: int, num_pages: int,
                  device=None, num_ctas: int | None = None, min_split_tokens: int = 256,
-                 max_splits: int = 64, policy: int = POLICY_BALANCED):
+                 max_splits: int = 64, policy: int = POLICY_BALANCED, groups: int = 1):
         self.device = torch.device(device if device is not None else "cuda")
         if num_ctas is None:
             num_ctas = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.shape = make_shape(R, k, H, max_pages, num_pages, num_ctas, min_split_tokens,
-                                max_splits, policy)
+                                max_splits, policy, groups)
         self.R, self.k, self.H, self.M = R, k, H, k * H
+        self.groups = groups
         i32 = dict(dtype=torch.int32, device=self.device)
-        self.counts = torch.zeros(R, **i32)
+        self.counts = torch.zeros(R * groups, **i32)
         self.work = torch.full((plan_list_len(self.shape),), -1, **i32)
         self.workspace = torch.empty(max(workspace_bytes(self.shape), 256), dtype=torch.uint8,
                                      device=self.device)

@@ -20,7 +20,8 @@ FAULT_WAIT_TIMEOUT, FAULT_PAGE_RANGE, FAULT_WORK_ITEM = 0x1, 0x2, 0x4
 
 # Every symbol include/mlafold.h declares.
 EXPORTS = ("mla_plan_list_len", "mla_workspace_bytes", "mla_plan_splits",
-           "mla_folded_decode", "mla_split_combine", "mla_folded_decode_noalloc")
+           "mla_folded_decode", "mla_split_combine", "mla_lse_merge",
+           "mla_folded_decode_noalloc")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -29,7 +30,7 @@ class MlaShape(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32),
                 ("num_pages", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
                 ("min_split_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32),
-                ("policy", ctypes.c_int32)]
+                ("policy", ctypes.c_int32), ("groups", ctypes.c_int32)]
 
 
 class MlaError(RuntimeError):
@@ -61,6 +62,8 @@ def load() -> ctypes.CDLL:
     lib.mla_folded_decode.restype = I32
     lib.mla_split_combine.argtypes = [SP, P, P, I32, P, SZ, F, P, P, P]
     lib.mla_split_combine.restype = I32
+    lib.mla_lse_merge.argtypes = [I32, I32, P, P, P, P, P]
+    lib.mla_lse_merge.restype = I32
     lib.mla_folded_decode_noalloc.argtypes = [SP, P, P, P, P, F, F, P, P, I32, P, P, P, P]
     lib.mla_folded_decode_noalloc.restype = I32
     _lib = lib

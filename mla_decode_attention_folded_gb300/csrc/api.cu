@@ -15,7 +15,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 int check_shape(const mla_shape* s) {
   if (!s) return MLA_ERR_NULL;
   if (s->page_size != kPage) return MLA_ERR_UNSUPPORTED;
-  if (s->R < 1 || s->R > kMaxR || s->k < 1 || s->H < 1) return MLA_ERR_SHAPE;
+  if (s->R < 1 || s->k < 1 || s->H < 1 || s->groups < 0) return MLA_ERR_SHAPE;
+  const int groups = s->groups > 0 ? s->groups : 1;
+  if (s->k % groups != 0 || (long long)s->R * groups > kMaxR) return MLA_ERR_SHAPE;
   const long long M = (long long)s->k * s->H;
   if (M > kMaxM) return MLA_ERR_SHAPE;
   if (s->max_pages < 1 || s->num_pages < 1 || s->num_pages >= (1 << 25)) return MLA_ERR_SHAPE;
@@ -88,7 +90,7 @@ int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
   if (workspace_bytes_given < need) return MLA_ERR_WORKSPACE;
   if (!std::isfinite(bmm1_scale) || !std::isfinite(bmm2_scale)) return MLA_ERR_SHAPE;
   if ((st = check_device()) != MLA_OK) return st;
-  const int M = shape->k * shape->H;
+  const int M = group_rows(*shape);
   const int slots = partial_slots(*shape);
   DecodeArgs a;
   a.q = static_cast<const uint8_t*>(q);
@@ -106,8 +108,9 @@ int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
   a.status = status;
   a.bmm1_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
   a.bmm2 = bmm2_scale;
-  a.R = shape->R;
+  a.R = plan_rows(*shape);
   a.M = M;
+  a.groups = shape_groups(*shape);
   a.max_pages = shape->max_pages;
   a.num_pages = shape->num_pages;
   a.list_len = list_len;
@@ -131,7 +134,7 @@ int32_t mla_split_combine(const mla_shape* shape, const int32_t* counts, const i
   if (workspace_bytes_given < need) return MLA_ERR_WORKSPACE;
   if (!std::isfinite(bmm2_scale)) return MLA_ERR_SHAPE;
   if ((st = check_device()) != MLA_OK) return st;
-  const int M = shape->k * shape->H;
+  const int M = group_rows(*shape);
   const int slots = partial_slots(*shape);
   if (slots == 0) return MLA_OK;       // no request can have two splits
   const float* po = static_cast<const float*>(workspace);
@@ -140,6 +143,20 @@ int32_t mla_split_combine(const mla_shape* shape, const int32_t* counts, const i
   cudaError_t e = launch_combine(*shape, counts, work, list_len, po, pl, slots, bmm2_scale,
                                  static_cast<uint16_t*>(out), lse,
                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_lse_merge(int32_t S, int32_t rows, const void* parts_out, const float* parts_lse,
+                      void* out, float* lse, mla_stream_t stream) {
+  if (!parts_out || !parts_lse || !out || !lse) return MLA_ERR_NULL;
+  if (S < 1 || S > 4096 || rows < 1) return MLA_ERR_SHAPE;
+  if (!aligned(parts_out, 16) || !aligned(out, 16) || !aligned(parts_lse, 4) || !aligned(lse, 4))
+    return MLA_ERR_ALIGN;
+  int st;
+  if ((st = check_device()) != MLA_OK) return st;
+  cudaError_t e = launch_lse_merge(S, rows, static_cast<const uint16_t*>(parts_out), parts_lse,
+                                   static_cast<uint16_t*>(out), lse,
+                                   reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -147,8 +147,8 @@ int reducer_bands(long long rows, int sms) {
 cudaError_t launch_combine(const mla_shape& s, const int32_t* counts, const int32_t* work,
                            int list_len, const float* part_o, const float* part_lse, int slots,
                            float bmm2, uint16_t* out, float* lse, cudaStream_t st) {
-  const int M = s.k * s.H;
-  const int bands = reducer_bands((long long)s.R * M, s.num_ctas);
+  const int M = group_rows(s), R = plan_rows(s);
+  const int bands = reducer_bands((long long)R * M, s.num_ctas);
   // Up to slots / 2 multi-split requests (each has two or more items).
   const long long rows = (long long)(slots / 2) * M * bands;
   long long blocks = cdiv(rows, kWarps);
@@ -165,9 +165,9 @@ cudaError_t launch_combine(const mla_shape& s, const int32_t* counts, const int3
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (bands == 2)
-    return cudaLaunchKernelEx(&cfg, combine_kernel<2>, counts, work, list_len, slots, s.R, M,
+    return cudaLaunchKernelEx(&cfg, combine_kernel<2>, counts, work, list_len, slots, R, M,
                               part_o, part_lse, bmm2, out, lse);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<1>, counts, work, list_len, slots, s.R, M,
+  return cudaLaunchKernelEx(&cfg, combine_kernel<1>, counts, work, list_len, slots, R, M,
                             part_o, part_lse, bmm2, out, lse);
 }
 

@@ -155,7 +155,7 @@ __device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, 
     return jb;
   }
   const int n = a.counts[r];
-  int L = max(a.seq_lens[r], 0);
+  int L = max(a.seq_lens[r / a.groups], 0);   // row group r reads request r / groups
   if (L > a.max_pages * kPage) {          // never read past the block-table row
     if (report && a.status) atomicOr(a.status, MLA_FAULT_PAGE_RANGE);
     L = a.max_pages * kPage;
@@ -195,7 +195,7 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
     const int end = (int)cdiv(jb.j1, kPage);
     int p = -1;
     if (first < end) {
-      p = a.block_table[(long long)jb.r * a.max_pages + first];
+      p = a.block_table[(long long)(jb.r / a.groups) * a.max_pages + first];
       if (p < 0 || p >= a.num_pages) {
         if (a.status) atomicOr(a.status, MLA_FAULT_PAGE_RANGE);
         p = -1;

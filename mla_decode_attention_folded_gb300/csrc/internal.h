@@ -33,25 +33,30 @@ __host__ __device__ inline int uniform_splits(int R, int M, int num_ctas, int ma
   if (s < 1) s = 1;
   return (int)(s < max_splits ? s : max_splits);
 }
+// Decode row groups (the planned "requests") and query rows per group.
+inline int shape_groups(const mla_shape& s) { return s.groups > 0 ? s.groups : 1; }
+inline int plan_rows(const mla_shape& s) { return s.R * shape_groups(s); }
+inline int group_rows(const mla_shape& s) { return (s.k / shape_groups(s)) * s.H; }
 inline int plan_list_len(const mla_shape& s) {
-  if (s.policy == MLA_POLICY_BALANCED) return plan_units(s.k * s.H, s.num_ctas) + s.R;
-  return s.R * uniform_splits(s.R, s.k * s.H, s.num_ctas, s.max_splits);
+  const int R = plan_rows(s), M = group_rows(s);
+  if (s.policy == MLA_POLICY_BALANCED) return plan_units(M, s.num_ctas) + R;
+  return R * uniform_splits(R, M, s.num_ctas, s.max_splits);
 }
 // Bound on items of multi-split requests; they occupy work-list slots [0, slots).
 inline int partial_slots(const mla_shape& s) {
-  int M = s.k * s.H;
+  const int R = plan_rows(s), M = group_rows(s);
   if (s.policy == MLA_POLICY_BALANCED) {
     int a = plan_list_len(s), b = 2 * plan_units(M, s.num_ctas);
     return a < b ? a : b;
   }
-  int u = uniform_splits(s.R, M, s.num_ctas, s.max_splits);
-  return u >= 2 ? s.R * u : 0;
+  int u = uniform_splits(R, M, s.num_ctas, s.max_splits);
+  return u >= 2 ? R * u : 0;
 }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Workspace: FP32 partial outputs [slots][M][512], then FP32 LSEs [slots][M].
 inline size_t partial_out_bytes(int slots, int M) { return align256(size_t(slots) * M * kDv * 4); }
 inline size_t workspace_bytes(const mla_shape& s) {
-  int slots = partial_slots(s), M = s.k * s.H;
+  int slots = partial_slots(s), M = group_rows(s);
   if (slots == 0) return 0;
   return partial_out_bytes(slots, M) + align256(size_t(slots) * M * 4);
 }
@@ -79,7 +84,8 @@ struct DecodeArgs {
   int32_t* status;   // may be null
   float bmm1_log2;   // bmm1_scale * log2(e)
   float bmm2;
-  int R, M, max_pages, num_pages, list_len, slots;
+  int R, M, max_pages, num_pages, list_len, slots;   // R, M: row groups, rows per group
+  int groups;          // row group g reads request g / groups
 };
 
 // Launchers (return cudaError_t of the launch).
@@ -89,5 +95,7 @@ cudaError_t launch_combine(const mla_shape& s, const int32_t* counts, const int3
                            int list_len, const float* part_o, const float* part_lse, int slots,
                            float bmm2, uint16_t* out, float* lse, cudaStream_t st);
 cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_lse_merge(int S, int rows, const uint16_t* parts_out, const float* parts_lse,
+                             uint16_t* out, float* lse, cudaStream_t st);
 
 }  // namespace mlafold

@@ -50,8 +50,8 @@ __device__ int block_max(int v, int* red) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-plan_kernel(const int32_t* __restrict__ seq_lens, int R, int M, int num_ctas, int minp,
-            int max_splits, int policy, int32_t* __restrict__ counts,
+plan_kernel(const int32_t* __restrict__ seq_lens, int R, int groups, int M, int num_ctas,
+            int minp, int max_splits, int policy, int32_t* __restrict__ counts,
             int32_t* __restrict__ work, int list_len) {
   __shared__ int s_len[kThreads];
   __shared__ int s_n_by_rank[kThreads];
@@ -62,7 +62,7 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int R, int M, int num_ctas, in
   grid_dep_wait();
   const int i = threadIdx.x;
   const bool live = i < R;
-  int L = live ? seq_lens[i] : 0;
+  int L = live ? seq_lens[i / groups] : 0;   // row group i reads request i / groups
   if (L < 0) L = 0;
   s_len[i] = live ? L : -1;               // dead slots rank after every request
   grid_dep_launch();                      // the decode may start its prologue
@@ -85,7 +85,15 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int R, int M, int num_ctas, in
       return block_sum<int>(mine, s_red);
     };
     if (Rn <= U && count(c) > U) {        // block-uniform branch
-      int lo = c + 1, hi = maxp;          // count(maxp) = Rn <= U
+      // Smallest chunk in (c, maxp] with at most U items (count(maxp) = Rn <= U;
+      // count never increases with the chunk). Gallop up from c, then bisect:
+      // the answer is usually within a step or two of c.
+      int lo = c + 1, hi = lo, step = 1;
+      while (hi < maxp && count(hi) > U) {
+        lo = hi + 1;
+        step *= 2;
+        hi = min(maxp, lo + step - 1);
+      }
       while (lo < hi) {
         const int mid = (lo + hi) / 2;
         if (count(mid) <= U) hi = mid; else lo = mid + 1;
@@ -153,7 +161,8 @@ cudaError_t launch_plan(const mla_shape& s, const int32_t* seq_lens, int32_t* co
                         int32_t* work, int list_len, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3((unsigned)((s.R + 31) / 32 * 32));   // one thread per request
+  const int R = plan_rows(s);
+  cfg.blockDim = dim3((unsigned)((R + 31) / 32 * 32));   // one thread per row group
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -161,8 +170,8 @@ cudaError_t launch_plan(const mla_shape& s, const int32_t* seq_lens, int32_t* co
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int minp = (int)cdiv(s.min_split_tokens, kPage) < 1 ? 1 : (int)cdiv(s.min_split_tokens, kPage);
-  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, s.R, s.k * s.H, s.num_ctas, minp,
-                            s.max_splits, s.policy, counts, work, list_len);
+  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, R, shape_groups(s), group_rows(s),
+                            s.num_ctas, minp, s.max_splits, s.policy, counts, work, list_len);
 }
 
 }  // namespace mlafold

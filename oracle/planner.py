@@ -131,6 +131,15 @@ def plan(seq_lens, M: int, num_ctas: int, min_split_tokens: int, max_splits: int
     return counts, out
 
 
+def fold_factor(k: int, heads: int, max_heads: int = 128) -> int:
+    """Query tokens folded into one decode row when a row may hold at most
+    `max_heads` heads: the largest divisor of k whose heads fit
+    (drafter-attention page, `fold_plan`, the LSE-returning route; 1 if even a
+    single token's heads do not fit)."""
+    fits = [d for d in range(1, k + 1) if k % d == 0 and d * heads <= max_heads]
+    return max(fits) if fits else 1
+
+
 def split_range(length: int, n: int, s: int) -> tuple[int, int]:
     """Keys [j0, j1) of split s of n of a request of ``length`` keys."""
     p = cdiv(length, PAGE)

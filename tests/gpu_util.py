@@ -32,8 +32,10 @@ def unfold(b):
 
 
 def run_decode(b, policy=mla.POLICY_BALANCED, num_ctas=None, folded=True,
-               min_split_tokens=256, max_splits=64, dev="cuda", d=None):
-    """-> (out [R, k*H, 512] float32 CPU, lse [R, k*H] CPU, status int, plan)."""
+               min_split_tokens=256, max_splits=64, dev="cuda", d=None, groups=1):
+    """-> (out [R, k*H, 512] float32 CPU, lse [R, k*H] CPU, status int, plan).
+    folded=False runs the stock flattened layout with replicated tables;
+    groups > 1 runs row groups of k/groups tokens on the request's own KV."""
     d = d or to_device(b, dev)
     if folded:
         R, k, H, bt, lens = b.R, b.k, b.H, d["bt"], d["lens"]
@@ -43,7 +45,8 @@ def run_decode(b, policy=mla.POLICY_BALANCED, num_ctas=None, folded=True,
     if num_ctas is None:
         num_ctas = torch.cuda.get_device_properties(dev).multi_processor_count
     eng = mla.FoldedMla(R, k, H, bt.shape[1], d["kv"].shape[0], dev, num_ctas=num_ctas,
-                        min_split_tokens=min_split_tokens, max_splits=max_splits, policy=policy)
+                        min_split_tokens=min_split_tokens, max_splits=max_splits, policy=policy,
+                        groups=groups if folded else 1)
     bmm1, bmm2 = bmm_scales(b)
     eng.plan(lens)
     out, lse = eng.decode(d["q"], d["kv"], bt, lens, bmm1, bmm2)

@@ -79,3 +79,34 @@ def test_short_list_and_workspace_rejected_before_any_launch():
     odd = ctypes.c_void_p((1 << 20) + 8)     # not 16-byte aligned
     args2 = [ctypes.byref(s), odd, fake, fake, fake, 1.0, 1.0, fake, fake]
     assert lib.mla_folded_decode(*args2, n, fake, 1 << 30, fake, fake, None, None) == -7
+
+
+def test_binding_fold_factor_matches_oracle():
+    for k in range(1, 13):
+        for H in (1, 8, 16, 64, 96, 128, 200):
+            assert mla.fold_factor(k, H, 128) == pl.fold_factor(k, H, 128)
+
+
+@pytest.mark.parametrize("R,k,H,groups", [(16, 4, 64, 2), (128, 7, 8, 7), (100, 6, 8, 3)])
+def test_row_group_sizes_match_oracle(R, k, H, groups):
+    for policy in (pl.BALANCED, pl.UNIFORM):
+        s = mla.make_shape(R, k, H, 10, 100, 152, 256, 64, policy, groups)
+        Rg, Mg = R * groups, (k // groups) * H
+        assert mla.plan_list_len(s) == pl.list_len(Rg, Mg, 152, policy, 64)
+        slots = pl.partial_slots(Rg, Mg, 152, policy, 64)
+        align = lambda x: (x + 255) // 256 * 256
+        want = 0 if slots == 0 else align(slots * Mg * 512 * 4) + align(slots * Mg * 4)
+        assert mla.workspace_bytes(s) == want
+
+
+@pytest.mark.parametrize("R,k,groups", [(4, 4, 3), (4, 6, 4), (600, 2, 2), (4, 2, -1)])
+def test_bad_row_groups_rejected(R, k, groups):
+    s = mla.make_shape(R, k, 8, 10, 100, 152, 256, 64, 0, groups)
+    assert _lib.load().mla_plan_list_len(ctypes.byref(s)) == -2
+
+
+def test_zero_groups_reads_as_one():
+    s0 = mla.make_shape(32, 4, 8, 10, 100, 152, 256, 64, 0, 0)
+    s1 = mla.make_shape(32, 4, 8, 10, 100, 152, 256, 64, 0, 1)
+    assert mla.plan_list_len(s0) == mla.plan_list_len(s1)
+    assert mla.workspace_bytes(s0) == mla.workspace_bytes(s1)

@@ -111,6 +111,44 @@ def test_small_cases_match_oracle(lens, k, H, policy):
             assert torch.all(out[i] == 0) and torch.all(torch.isneginf(lse[i]))
 
 
+def test_planner_bit_exact_with_row_groups():
+    rng = np.random.default_rng(7)
+    for trial in range(300):
+        R = int(rng.integers(1, 120))
+        k = int(rng.choice([2, 4, 6, 7, 8]))
+        groups = int(rng.choice([d for d in range(1, k + 1) if k % d == 0]))
+        if R * groups > 1024:
+            continue
+        H = int(rng.choice([8, 16, 64]))
+        lens = rng.integers(0, 20000, size=R)
+        G = int(rng.choice([8, 152]))
+        policy = int(rng.integers(0, 2))
+        s = mla.make_shape(R, k, H, 1, 1, G, 256, 64, policy, groups)
+        n = mla.plan_list_len(s)
+        counts = torch.zeros(R * groups, dtype=torch.int32, device="cuda")
+        work = torch.full((n,), 7, dtype=torch.int32, device="cuda")
+        mla.plan_splits(s, torch.tensor(lens.astype(np.int32), device="cuda"), counts, work)
+        c2, w2 = pl.plan(np.repeat(lens, groups), (k // groups) * H, G, 256, 64, policy)
+        assert np.array_equal(counts.cpu().numpy(), c2), trial
+        assert np.array_equal(work.cpu().numpy(), w2), trial
+
+
+@pytest.mark.parametrize("lens,k,H", [((900, 77, 2000), 4, 64), ((1500, 300), 7, 8),
+                                      ((700, 0, 64), 6, 16)])
+def test_row_groups_match_oracle(lens, k, H):
+    """Unfolded (groups = k), the pages' partial fold and every divisor in
+    between give the same attention as the oracle."""
+    b = make_batch_from_lengths(lens, k, H, seed=sum(lens) + k, scaling="amax", fill=-5)
+    ref_o, ref_l = oracle_full(b)
+    divisors = [g for g in range(1, k + 1) if k % g == 0]
+    assert k // mla.fold_factor(k, H) in divisors
+    for groups in divisors:
+        for policy in (pl.BALANCED, pl.UNIFORM):
+            out, lse, status, _ = run_decode(b, policy=policy, groups=groups, min_split_tokens=64)
+            assert status == 0
+            assert_close(out, lse, ref_o, ref_l, f"groups={groups} policy={policy}")
+
+
 def test_folded_equals_unfolded():
     b = make_batch_from_lengths((900, 77, 2000), 4, 8, seed=5, scaling="amax")
     ref_o, ref_l = oracle_full(b)

@@ -133,3 +133,22 @@ def test_skewed_batch_balances_better_than_uniform():
     largest_b = max(-(-p // cb))
     largest_u = max(-(-p // cu))
     assert largest_u >= 1.5 * largest_b
+
+
+def test_fold_factor_worked_example():
+    """The pages' example: k = 4 at 64 heads with a 128-head cap folds pairs."""
+    for line in open(os.path.join(GOLDEN, "fold_plan_example.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, H, cap, want = (int(x) for x in line.split())
+        assert pl.fold_factor(k, H, cap) == want
+
+
+@pytest.mark.parametrize("k", range(1, 13))
+@pytest.mark.parametrize("H", [1, 8, 16, 64, 96, 128, 200])
+def test_fold_factor_properties(k, H):
+    f = pl.fold_factor(k, H, 128)
+    assert k % f == 0
+    assert f == 1 or f * H <= 128
+    assert all(not (k % d == 0 and d * H <= 128) for d in range(f + 1, k + 1))

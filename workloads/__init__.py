@@ -173,3 +173,26 @@ def make_batch(name: str, *, fill: int = 0) -> Batch:
     return make_batch_from_lengths(lens, w.k, w.H, seed=w.seed + 7919, value_std=w.value_std,
                                    scaling=w.scaling, fill=fill)
 
+
+
+def shard_pages(batch: Batch, shards: int, shard: int) -> Batch:
+    """The part of `batch` that shard `shard` of `shards` holds when each
+    request's KV pages are interleaved over the shards page by page (page p of
+    a request lives on shard p % shards), as a decode-context-parallel cache
+    is laid out. Queries and the cache buffer are shared; the block table and
+    lengths are the shard's local ones (its pages in order; only a request's
+    last page can be partial, and it is also the last page of its shard)."""
+    lens = batch.seq_lens.numpy().astype(np.int64)
+    bt = batch.block_table.numpy()
+    R = lens.size
+    local_pages = [list(range(shard, int((L + PAGE - 1) // PAGE), shards)) for L in lens]
+    width = max(1, max(len(p) for p in local_pages))
+    lbt = np.zeros((R, width), dtype=np.int32)
+    llen = np.zeros(R, dtype=np.int32)
+    for r, pages in enumerate(local_pages):
+        for j, p in enumerate(pages):
+            lbt[r, j] = bt[r, p]
+            llen[r] += min(PAGE, int(lens[r]) - PAGE * p)
+    return Batch(q=batch.q, kv=batch.kv, block_table=torch.from_numpy(lbt),
+                 seq_lens=torch.from_numpy(llen), k=batch.k, H=batch.H,
+                 q_scale=batch.q_scale, kv_scale=batch.kv_scale, sm_scale=batch.sm_scale)
