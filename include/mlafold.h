@@ -135,7 +135,7 @@ int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t
  *   block_table [R, max_pages] int32, device: page ids; only the first
  *               ceil(seq_lens[r] / 64) entries of row r are read.
  *   seq_lens    [R] int32, device: the same lengths that were planned.
- *   bmm1_scale  sm_scale * q_scale * kv_scale; bmm2_scale: kv_scale.
+ *   bmm1_scale  sm_scale * q_scale * kv_scale, finite and > 0; bmm2_scale: kv_scale.
  *   counts/work the plan of mla_plan_splits for these lengths; list_len its size.
  *   workspace   >= mla_workspace_bytes(shape) bytes, device, 256-byte aligned;
  *               scratch for split partials (contents need not be initialised).

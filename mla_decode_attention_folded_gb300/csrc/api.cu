@@ -88,7 +88,8 @@ int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
     return MLA_ERR_ALIGN;
   if (list_len < plan_list_len(*shape)) return MLA_ERR_LIST;
   if (workspace_bytes_given < need) return MLA_ERR_WORKSPACE;
-  if (!std::isfinite(bmm1_scale) || !std::isfinite(bmm2_scale)) return MLA_ERR_SHAPE;
+  if (!std::isfinite(bmm1_scale) || !(bmm1_scale > 0.f) || !std::isfinite(bmm2_scale))
+    return MLA_ERR_SHAPE;
   if ((st = check_device()) != MLA_OK) return st;
   const int M = group_rows(*shape);
   const int slots = partial_slots(*shape);

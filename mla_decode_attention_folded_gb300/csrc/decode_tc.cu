@@ -28,27 +28,12 @@
 // * Every mbarrier wait is bounded (2 s); on expiry the CTA sets
 //   MLA_FAULT_WAIT_TIMEOUT in the status word, stops, drains its own copies and
 //   MMAs, frees TMEM and returns. No trap, no unbounded spin.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "internal.h"
-#include "ptx.cuh"
-#include "tc.cuh"
+#include "decode_common.cuh"
 
 namespace mlafold {
 namespace {
 
-constexpr int kTileKeys = 128;                    // keys per MMA tile (two pages)
-constexpr int kStages = 2;                        // KV tiles in flight
-constexpr int kThreads = 192;                     // 6 warps
-constexpr int kChunkBytes = kTileKeys * 128;      // one 128-dim latent band of a tile
-constexpr int kRopeBytes = kTileKeys * 64;        // the 64 rope dims of a tile
-constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;     // 73728
-constexpr int kPageBytes = kPage * kDqk;          // 36864 bytes per page
-constexpr int kOCols = 64;                        // TMEM columns per 128-dim band of O^T
-constexpr int kSCol0 = 4 * kOCols;                // S^T buffers start after O^T
-constexpr uint32_t kTmemCols = 512;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
+using namespace dec;
 
 template <int NR>
 struct Cfg {
@@ -64,38 +49,6 @@ struct Cfg {
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1 KB alignment");
   static_assert(kSCol0 + 2 * NR <= (int)kTmemCols, "TMEM budget");
 };
-
-struct Ctl {
-  uint64_t kv_full[kStages];   // TMA -> MMA: tile landed
-  uint64_t pv_done[kStages];   // MMA -> TMA, softmax: PV of a tile finished (stage, P free)
-  uint64_t s_full[2];          // MMA -> softmax: S^T ready
-  uint64_t s_empty[2];         // softmax -> MMA: S^T read
-  uint64_t p_full[2];          // softmax -> MMA: P^T written, masked V rows zeroed
-  uint64_t q_full, q_empty;    // Q block of the job
-  uint64_t o_full, o_empty;    // O^T of the job
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  float m_run[64];             // running row max (base-2 scores)
-  float vec[64];               // rescale factors, then 1/l
-  float lse[64];
-  float red[4][64];            // cross-warp reduction scratch
-};
-
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ctl,
-                                         int32_t* status) {
-  if (tc::mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = tc::globaltimer_ns();
-  while (true) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
-    if (tc::globaltimer_ns() - t0 > kTimeoutNs) {
-      *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
-      if (status) atomicOr(status, MLA_FAULT_WAIT_TIMEOUT);
-      return false;
-    }
-  }
-}
 
 // Reduce v[32] across the 32 lanes by halving exchanges (31 shuffles per
 // lane instead of 160); afterwards lane l holds the reduction of row l in v[0].
@@ -117,149 +70,6 @@ __device__ __forceinline__ void transpose_reduce32(float* v, int lane) {
   tr_step<8, MAX>(v, lane, 4);
   tr_step<4, MAX>(v, lane, 2);
   tr_step<2, MAX>(v, lane, 1);
-}
-
-__device__ __forceinline__ void group_sync() {   // the 128 softmax threads
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-__device__ __forceinline__ bool group_any(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, 2, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r)
-      : "r"((uint32_t)pred)
-      : "memory");
-  return r != 0;
-}
-
-// Per-job facts every role derives identically from the plan.
-struct Job {
-  int r, blk, item, j0, j1, ntiles;
-  bool direct, skip;
-};
-
-__device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, bool report) {
-  Job jb;
-  jb.item = item;
-  jb.blk = blk;
-  jb.skip = false;
-  const int e = a.work[item];
-  const int r = e >> kSplitBits, s = e & ((1 << kSplitBits) - 1);
-  jb.r = r;
-  if (r >= a.R || s >= a.counts[r]) {
-    if (report && a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
-    jb.skip = true;
-    jb.j0 = jb.j1 = jb.ntiles = 0;
-    jb.direct = false;
-    return jb;
-  }
-  const int n = a.counts[r];
-  int L = max(a.seq_lens[r / a.groups], 0);   // row group r reads request r / groups
-  if (L > a.max_pages * kPage) {          // never read past the block-table row
-    if (report && a.status) atomicOr(a.status, MLA_FAULT_PAGE_RANGE);
-    L = a.max_pages * kPage;
-  }
-  split_range(L, n, s, jb.j0, jb.j1);
-  jb.ntiles = (int)cdiv(jb.j1 - jb.j0, kTileKeys);
-  jb.direct = n == 1;
-  if (!jb.direct && item >= a.slots) {
-    if (report && a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
-    jb.skip = true;
-  }
-  return jb;
-}
-
-// ---------------------------------------------------------------- producer
-// Runs on all 32 lanes of warp 0: the lanes fetch the job's block-table
-// entries 32 at a time (lane i holds page i of the chunk, checked against the
-// cache), lane 0 waits on the ring and issues the TMA copies.
-template <int NR>
-__device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
-                         const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
-                         const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
-  using C = Cfg<NR>;
-  const int lane = threadIdx.x & 31;
-  uint32_t g = 0, x = 0;
-  int last_q_parity = -1;
-  int last_kv_parity[kStages] = {-1, -1};
-  const int njobs = a.list_len * nb;
-  bool ok = true;
-  auto wait0 = [&](uint64_t* bar, uint32_t parity) {
-    int r = 1;
-    if (lane == 0) r = wait_bar(bar, parity, ctl, a.status) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, r, 0) != 0;
-  };
-  auto fetch = [&](const Job& jb, int chunk) {   // page ids of job pages 32*chunk + lane
-    const int first = jb.j0 / kPage + chunk * 32 + lane;
-    const int end = (int)cdiv(jb.j1, kPage);
-    int p = -1;
-    if (first < end) {
-      p = a.block_table[(long long)(jb.r / a.groups) * a.max_pages + first];
-      if (p < 0 || p >= a.num_pages) {
-        if (a.status) atomicOr(a.status, MLA_FAULT_PAGE_RANGE);
-        p = -1;
-      }
-    }
-    return p;
-  };
-  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
-    const int item = job / nb, blk = job % nb;
-    if (a.work[item] < 0) break;
-    const Job jb = read_job(a, item, blk, lane == 0);
-    if (jb.skip || jb.ntiles == 0) continue;
-    int cur = fetch(jb, 0), nxt = fetch(jb, 1);
-    if (x > 0 && !(ok = wait0(&ctl->q_empty, (x - 1) & 1))) break;
-    if (lane == 0) {
-      uint8_t* q = smem + C::kOffQ;
-      tc::mbar_arrive_expect_tx(&ctl->q_full, C::kQBytes);
-      for (int c = 0; c < 4; ++c)
-        tc::tma_load_3d(q + c * C::kQChunk, tm_q, &ctl->q_full, c * 128, blk * NR, jb.r);
-      tc::tma_load_3d(q + 4 * C::kQChunk, tm_qr, &ctl->q_full, 512, blk * NR, jb.r);
-    }
-    last_q_parity = x & 1;
-    for (int t = 0; t < jb.ntiles; ++t, ++g) {
-      if (t > 0 && (t & 15) == 0) {            // 16 tiles = 32 pages per chunk
-        cur = nxt;
-        nxt = fetch(jb, (t >> 4) + 1);
-      }
-      const int st = g & 1;
-      if (g >= 2 && !(ok = wait0(&ctl->pv_done[st], ((g >> 1) - 1) & 1))) break;
-      const int kbase = jb.j0 + t * kTileKeys;
-      const int pages = (kbase + kPage < jb.j1) ? 2 : 1;
-      const int pid0 = __shfl_sync(0xffffffffu, cur, (2 * t) & 31);
-      const int pid1 = __shfl_sync(0xffffffffu, cur, (2 * t + 1) & 31);
-      if (lane == 0) {
-        const int pid[2] = {pid0, pages == 2 ? pid1 : -1};
-        const int nvalid = (pid[0] >= 0) + (pid[1] >= 0);
-        uint8_t* stage = smem + st * kStageBytes;
-        tc::mbar_arrive_expect_tx(&ctl->kv_full[st], nvalid * kPageBytes);
-        for (int h = 0; h < 2; ++h) {
-          if (pid[h] < 0) continue;
-          const int row = pid[h] * kPage;
-          for (int c = 0; c < 4; ++c)
-            tc::tma_load_2d(stage + c * kChunkBytes + h * (kChunkBytes / 2), tm_kv,
-                            &ctl->kv_full[st], c * 128, row);
-          tc::tma_load_2d(stage + 4 * kChunkBytes + h * (kRopeBytes / 2), tm_kvr,
-                          &ctl->kv_full[st], 512, row);
-        }
-      }
-      last_kv_parity[st] = (g >> 1) & 1;
-    }
-    ++x;
-  }
-  // Never leave with copies in flight into this CTA's shared memory.
-  if (!ok && lane == 0) {
-    const unsigned long long t0 = tc::globaltimer_ns();
-    for (int st = 0; st < kStages; ++st)
-      while (last_kv_parity[st] >= 0 &&
-             !tc::mbar_try_wait(&ctl->kv_full[st], last_kv_parity[st]) &&
-             tc::globaltimer_ns() - t0 < kTimeoutNs) {
-      }
-    while (last_q_parity >= 0 && !tc::mbar_try_wait(&ctl->q_full, last_q_parity) &&
-           tc::globaltimer_ns() - t0 < kTimeoutNs) {
-    }
-  }
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -385,22 +195,6 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
-__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
-  return r;
-}
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // Copy one staged 128-dim band of `rows` rows (BF16 out or FP32 partial) to
 // global memory as 16-byte row vectors; the 128 group threads stride the
 // chunks, fully unrolled so the loads pipeline.
@@ -706,7 +500,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
   grid_dep_wait();      // the plan is complete; earlier readers of out/workspace are done
   grid_dep_launch();    // the reducer may launch; it still waits for this grid to finish
   if (warp == 0) {
-    producer<NR>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
+    producer<NR, 1, Cfg<NR>::kOffQ>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer<NR>(a, smem, ctl, tmem, nb);
   } else {
@@ -719,29 +513,6 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int NR>
 cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<NR>;
@@ -759,15 +530,8 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
     return cudaErrorInvalidValue;
   const int smem_bytes = C::kOffCtl + (int)sizeof(Ctl) + 1024;
   static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = set_smem(decode_tc_kernel<NR>, smem_bytes, attr_set);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
   const int nb = row_blocks(a.M);
   const long long jobs = (long long)a.list_len * nb;
   const int grid = (int)(jobs < s.num_ctas ? jobs : s.num_ctas);
@@ -787,6 +551,7 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
 }  // namespace
 
 cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
+  if (rows_as_m(a.M)) return launch_decode_rows(s, a, st);   // query rows as the MMA's M
   return row_block(a.M) == 32 ? launch_nr<32>(s, a, st) : launch_nr<64>(s, a, st);
 }
 

@@ -92,6 +92,10 @@ CASES = [
     ((1500,), 1, 64),
     ((900, 130), 2, 40),
     ((2500, 64), 4, 64),
+    ((2100, 640), 7, 64),
+    ((500, 70), 2, 65),
+    ((1300, 90), 6, 64),
+    ((800, 200), 15, 32),
 ]
 
 
