@@ -38,7 +38,8 @@ METRIC = "decode rows/s and KV HBM GB/s (fraction of 8 TB/s) vs unfolded, 1 GB30
 UNIT = "rows/s"
 DEFAULT_WORKLOAD = "R32_k4_H8_len1k-8k"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ("decode_tc.cu", "internal.h", "ptx.cuh", "tc.cuh")
+DECODE_SOURCES = ("decode_tc.cu", "decode_rows.cu", "decode_common.cuh", "internal.h", "ptx.cuh",
+                  "tc.cuh")
 
 
 def parse():

@@ -114,8 +114,9 @@ __device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, 
 // entries 32 at a time (lane i holds page i of the chunk, checked against the
 // cache), lane 0 waits on the ring and issues the TMA copies.
 // QROWS: query rows per Q block; SHARE: consecutive jobs of an item that
-// use the same Q block; OFFQ: shared-memory offset of the Q block.
-template <int QROWS, int SHARE, int OFFQ>
+// use the same Q block; OFFQ: shared-memory offset of the Q block; STAGGER:
+// request the CTA's second tile only once its first has landed.
+template <int QROWS, int SHARE, int OFFQ, bool STAGGER>
 __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
                          const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
                          const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
@@ -167,6 +168,11 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
       }
       const int st = g & 1;
       if (g >= 2 && !(ok = wait0(&ctl->pv_done[st], ((g >> 1) - 1) & 1))) break;
+      // Every CTA starts at once. With short, HBM-bound jobs it pays to ask
+      // for the second tile only after the first has landed: the first tiles
+      // then arrive first and the MMAs start while the second ones stream in,
+      // instead of both arriving together.
+      if (STAGGER && g == 1 && !(ok = wait0(&ctl->kv_full[0], 0))) break;
       const int kbase = jb.j0 + t * kTileKeys;
       const int pages = (kbase + kPage < jb.j1) ? 2 : 1;
       const int pid0 = __shfl_sync(0xffffffffu, cur, (2 * t) & 31);
