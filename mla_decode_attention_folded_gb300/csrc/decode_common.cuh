@@ -115,8 +115,10 @@ __device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, 
 // cache), lane 0 waits on the ring and issues the TMA copies.
 // QROWS: query rows per Q block; SHARE: consecutive jobs of an item that
 // use the same Q block; OFFQ: shared-memory offset of the Q block; STAGGER:
-// request the CTA's second tile only once its first has landed.
-template <int QROWS, int SHARE, int OFFQ, bool STAGGER>
+// request the CTA's second tile only once its first has landed; PREFETCH:
+// with each tile, warm L2 with the pages of the tile that will next use the
+// same stage.
+template <int QROWS, int SHARE, int OFFQ, bool STAGGER, bool PREFETCH>
 __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
                          const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
                          const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
@@ -193,6 +195,19 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
         }
       }
       last_kv_parity[st] = (g >> 1) & 1;
+      // Tile t + kStages is requested only once PV(t) frees this stage; warmed
+      // in L2 now, its copy then skips most of the HBM latency.
+      if (PREFETCH && t + kStages < jb.ntiles) {
+        const int tp = t + kStages;
+        const int src = (tp >> 4) == (t >> 4) ? cur : nxt;
+        const int q0 = __shfl_sync(0xffffffffu, src, (2 * tp) & 31);
+        const int q1 = __shfl_sync(0xffffffffu, src, (2 * tp + 1) & 31);
+        if (lane == 0) {
+          if (q0 >= 0) tc::prefetch_l2(a.kv + (size_t)q0 * kPageBytes, kPageBytes);
+          if (q1 >= 0 && jb.j0 + tp * kTileKeys + kPage < jb.j1)
+            tc::prefetch_l2(a.kv + (size_t)q1 * kPageBytes, kPageBytes);
+        }
+      }
     }
     ++x;
   }

@@ -372,7 +372,7 @@ decode_rows_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv
   grid_dep_wait();      // the plan is complete; earlier readers of out/workspace are done
   grid_dep_launch();    // the reducer may launch; it still waits for this grid to finish
   if (warp == 0) {
-    producer<kQRows, 2, kOffQ, false>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
+    producer<kQRows, 2, kOffQ, false, true>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
   } else if (warp == 1) {
     if (lane == 0) rows_mma_issuer(a, smem, ctl, tmem, nb);
   } else {

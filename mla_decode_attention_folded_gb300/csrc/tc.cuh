@@ -66,6 +66,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2; no
+// completion to wait for and nothing written to shared memory.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar,
                                             int x, int y) {
   asm volatile(
