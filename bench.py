@@ -37,6 +37,7 @@ from workloads import D_QK, WORKLOADS, make_batch  # noqa: E402
 METRIC = "decode rows/s and KV HBM GB/s (fraction of 8 TB/s) vs unfolded, 1 GB300"
 UNIT = "rows/s"
 DEFAULT_WORKLOAD = "R32_k4_H8_len1k-8k"
+REFERENCE_BUDGET_S = 120.0
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ("decode_tc.cu", "decode_rows.cu", "decode_common.cuh", "internal.h", "ptx.cuh",
                   "tc.cuh")
@@ -63,22 +64,46 @@ def dist_env():
 
 
 # ---------------------------------------------------------------- oracle timing
-def oracle_rows_per_s(batch, seconds: float):
-    """Time the CPU oracle, as it stands, on whole requests of the batch until
-    ``seconds`` of CPU work have passed. Returns (rows/s, requests, elapsed)."""
-    import oracle.attention as att
-    lens = batch.seq_lens.numpy()
-    order = list(range(batch.R))
-    done, t0 = 0, time.perf_counter()
-    while done < len(order):
-        r = order[done]
-        att.mla_decode(batch.q.numpy(), batch.kv.numpy(), batch.block_table.numpy(), lens,
-                       batch.k, batch.sm_scale, batch.q_scale, batch.kv_scale, requests=[r])
-        done += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    el = time.perf_counter() - t0
-    return done * batch.k / el, done, el
+class OracleSampler:
+    """Times the CPU oracle, as it stands, on consecutive 256-key chunks of the
+    batch's requests (request by request, cycling). A chunk of c keys of a
+    request of L keys is c / L of that request's k query-token rows, so the
+    rate is in the headline unit whatever the sample size; the merge of the
+    chunks (negligible work) is not run."""
+    CHUNK = 256
+
+    def __init__(self, batch):
+        import oracle.attention as att
+        self.att = att
+        self.b = batch
+        self.q, self.kv = batch.q.numpy(), batch.kv.numpy()
+        self.bt, self.lens = batch.block_table.numpy(), batch.seq_lens.numpy()
+        self.ranges = np.zeros((batch.R, 2), dtype=np.int64)
+        self.r, self.j = 0, 0
+        if int(self.lens.max(initial=0)) <= 0:
+            raise ValueError("every request is empty")
+
+    def run(self, seconds: float):
+        """At least one chunk, then chunks until `seconds` have passed.
+        Returns (rows/s, rows, elapsed s, chunks)."""
+        b, rows, chunks = self.b, 0.0, 0
+        t0 = time.perf_counter()
+        while True:
+            L = int(self.lens[self.r])
+            if L > 0:
+                j1 = min(L, self.j + self.CHUNK)
+                self.ranges[self.r] = (self.j, j1)
+                self.att.mla_decode(self.q, self.kv, self.bt, self.lens, b.k, b.sm_scale,
+                                    b.q_scale, b.kv_scale, key_range=self.ranges,
+                                    requests=[self.r])
+                rows += (j1 - self.j) / L * b.k
+                chunks += 1
+                self.j = j1
+            if L <= 0 or self.j >= L:
+                self.r, self.j = (self.r + 1) % b.R, 0
+            el = time.perf_counter() - t0
+            if chunks > 0 and el >= seconds:
+                return rows / el, rows, el, chunks
 
 
 def cpu_threads() -> int:
@@ -426,10 +451,11 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rps, nreq, el = oracle_rows_per_s(batch, args.cpu_seconds)
+        rps, rows, el, chunks = OracleSampler(batch).run(args.cpu_seconds)
         cpu = {"value": rps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-               "sample": f"{nreq} of {batch.R} requests of {args.workload} "
-                         f"({el:.1f} s, float64 numpy)"}
+               "sample": f"{chunks} consecutive {OracleSampler.CHUNK}-key chunks of the "
+                         f"requests of {args.workload} = {rows:.1f} of {batch.R * batch.k} "
+                         f"query-token rows ({el:.1f} s, float64 numpy)"}
 
     if rank != 0:
         return
@@ -468,25 +494,30 @@ def run_reference(args):
     if rank != 0:
         return
     batch = make_batch(args.workload)
-    per_step = max(1.0, min(args.cpu_seconds, 240.0 / max(1, args.steps + args.warmup)))
+    sampler = OracleSampler(batch)
+    # The whole run (warm-up included) targets about REFERENCE_BUDGET_S of CPU
+    # work; each step runs at least one chunk.
+    per_step = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
     for _ in range(args.warmup):
-        oracle_rows_per_s(batch, per_step)
-    vals, reqs = [], []
+        sampler.run(per_step)
+    rows_t, el_t, chunks_t = 0.0, 0.0, 0
     for _ in range(args.steps):
-        v, n, _ = oracle_rows_per_s(batch, per_step)
-        vals.append(v)
-        reqs.append(n)
-    value = statistics.mean(vals)
+        _, rows, el, chunks = sampler.run(per_step)
+        rows_t, el_t, chunks_t = rows_t + rows, el_t + el, chunks_t + chunks
+    value = rows_t / el_t
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": args.workload, "R": batch.R, "k": batch.k, "H": batch.H,
                    "M": batch.M},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"each step: whole requests of {args.workload} for "
-                                   f"{per_step:.1f} s ({min(reqs)}-{max(reqs)} requests)"},
+                         "sample": f"each step: consecutive {OracleSampler.CHUNK}-key chunks of "
+                                   f"the requests of {args.workload} for about "
+                                   f"{per_step * 1e3:.0f} ms (at least one chunk); "
+                                   f"{chunks_t} chunks = {rows_t:.1f} query-token rows "
+                                   f"over the timed steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
