@@ -454,8 +454,8 @@ def run_ours(args):
         rps, rows, el, chunks = OracleSampler(batch).run(args.cpu_seconds)
         cpu = {"value": rps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                "sample": f"{chunks} consecutive {OracleSampler.CHUNK}-key chunks of the "
-                         f"requests of {args.workload} = {rows:.1f} of {batch.R * batch.k} "
-                         f"query-token rows ({el:.1f} s, float64 numpy)"}
+                         f"requests of {args.workload} = {rows:.1f} query-token rows (the batch "
+                         f"has {batch.R * batch.k}; {el:.1f} s, float64 numpy)"}
 
     if rank != 0:
         return
