@@ -39,6 +39,7 @@ UNIT = "rows/s"
 DEFAULT_WORKLOAD = "R32_k4_H8_len1k-8k"
 REFERENCE_BUDGET_S = 120.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 DECODE_SOURCES = ("decode_tc.cu", "decode_rows.cu", "decode_common.cuh", "internal.h", "ptx.cuh",
                   "tc.cuh")
 
@@ -225,6 +226,43 @@ def measured_hbm_peak():
         return v, "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def fp8_tensor_peak():
+    """Dense FP8 TFLOP/s: the measured burst bf16 GEMM rate times the nominal
+    FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        v = float(json.load(open(path))["bf16_tflops"])
+        return 2.0 * v, "measured bf16 x nominal fp8/bf16 ratio 2"
+    except (OSError, KeyError, ValueError):
+        return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x nominal fp8/bf16 ratio 2"
+
+
+def algorithmic_flops(lens, M: int) -> int:
+    """S = Q.K^T over 576 dims and O = P.V over 512 dims: 2 * M * len * 1088."""
+    return int(2 * M * (D_QK + 512) * np.asarray(lens, dtype=np.int64).sum())
+
+
+def roofline(algo_bytes: int, flops: int, kernel_s: float):
+    """The bound that binds at this arithmetic intensity (HBM below the ridge
+    of the two measured peaks, the FP8 tensor pipe above it), with both
+    fractions."""
+    hbm, hbm_src = measured_hbm_peak()
+    fp8, fp8_src = fp8_tensor_peak()
+    gbs = algo_bytes / kernel_s / 1e9
+    tfs = flops / kernel_s / 1e12
+    ridge = fp8 * 1e12 / (hbm * 1e9)
+    intensity = flops / algo_bytes
+    r = {"hbm_frac": gbs / hbm, "tensor_frac": tfs / fp8,
+         "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge}
+    if intensity < ridge:
+        r.update(bound="hbm", achieved=gbs, peak=hbm, unit="GB/s", frac=gbs / hbm,
+                 peak_source=hbm_src)
+    else:
+        r.update(bound="tensor", achieved=tfs, peak=fp8, unit="TFLOP/s", frac=tfs / fp8,
+                 peak_source=fp8_src)
+    return r
 
 
 class Runner:
@@ -429,8 +467,8 @@ def run_ours(args):
     kv_b = D_QK * int(lens.sum())
     value = world * rows / (step_ms / 1e3)
     algo = algorithmic_bytes(lens, batch.M)
-    peak, peak_src = measured_hbm_peak()
-    achieved = algo / (dec_ms / 1e3) / 1e9
+    flops = algorithmic_flops(lens, batch.M)
+    roof = roofline(algo, flops, dec_ms / 1e3)
 
     variants = {}
     if rank == 0 and not args.no_variants:
@@ -475,10 +513,9 @@ def run_ours(args):
         "kernel_ms": {"plan": plan_ms, "decode": dec_ms, "combine": comb_ms},
         "chain_ms": {"step": step_ms, "without_plan": no_plan_ms, "without_combine": no_comb_ms},
         "variants": variants,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_src,
-                     "traffic": profiled_traffic(args.workload),
-                     "kernel": "mla_folded_decode", "algorithmic_bytes_per_launch": algo},
+        "roofline": dict(roof, traffic=profiled_traffic(args.workload),
+                         kernel="mla_folded_decode", algorithmic_bytes_per_launch=algo,
+                         algorithmic_flops_per_launch=flops),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_v, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

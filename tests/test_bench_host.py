@@ -34,3 +34,16 @@ def test_algorithmic_bytes_formula():
     got = bench.algorithmic_bytes(lens, M)
     want = 576 * lens.sum() + len(lens) * M * (576 + 1028) + 4 * pages
     assert got == want
+
+
+def test_roofline_picks_binding_bound():
+    hbm, _ = bench.measured_hbm_peak()
+    fp8, _ = bench.fp8_tensor_peak()
+    ridge = fp8 * 1e12 / (hbm * 1e9)
+    lo = bench.roofline(10**9, int(0.5 * ridge * 10**9), 1e-3)
+    hi = bench.roofline(10**9, int(2.0 * ridge * 10**9), 1e-3)
+    assert lo["bound"] == "hbm" and lo["unit"] == "GB/s"
+    assert lo["achieved"] == pytest.approx(1000.0) and lo["frac"] == pytest.approx(1000.0 / hbm)
+    assert hi["bound"] == "tensor" and hi["unit"] == "TFLOP/s"
+    assert hi["frac"] == pytest.approx(hi["achieved"] / fp8)
+    assert bench.algorithmic_flops([100, 28], 3) == 2 * 3 * 1088 * 128
