@@ -141,7 +141,10 @@ int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t
  *               scratch for split partials (contents need not be initialised).
  *   out         [R, M, 512] BF16, device, 16-byte aligned, written for requests
  *               with one split (the others are written by mla_split_combine).
- *   lse         [R, M] FP32 base-2 LSE, device, written like `out`.
+ *   lse         [R, M] FP32 base-2 LSE, device, written like `out`; or NULL for
+ *               the route without an LSE (drafter-attention page, `fold_plan`
+ *               and `draft_forward_mqa` with return_lse off): nothing is
+ *               written for it (split partials still carry their own LSEs).
  *   status      optional int32 device word (may be NULL); the kernel ORs in
  *               MLA_FAULT_* bits for conditions it detects instead of trapping.
  * Numerics: FP8 QK^T and PV on the tensor cores with FP32 accumulation; FP32
@@ -160,7 +163,8 @@ int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
  * with two or more splits: out = bmm2_scale * sum_s w_s O_s / sum_s w_s, with
  * w_s = 2^(lse_s - max_s lse_s), rounded once to BF16; lse = max + log2 sum w
  * (drafter-attention page, `DraftDcp`: exp2(lse - max) / sum in FP32, one
- * BF16 rounding). Arguments as for mla_folded_decode, same plan and workspace.
+ * BF16 rounding). Arguments as for mla_folded_decode, same plan and workspace
+ * (lse may be NULL: no LSE written).
  * Rows whose splits are all empty get out = 0 and lse = -inf. */
 int32_t mla_split_combine(const mla_shape *shape, const int32_t *counts, const int32_t *work,
                           int32_t list_len, const void *workspace, size_t workspace_bytes,
@@ -174,7 +178,8 @@ int32_t mla_split_combine(const mla_shape *shape, const int32_t *counts, const i
  *   lse = max + log2 sum_s w_s; rows whose sources are all empty get 0, -inf.
  *   parts_out [S, rows, 512] BF16, device, 16-byte aligned: each source's out.
  *   parts_lse [S, rows] FP32 base-2 LSE, device.
- *   out [rows, 512] BF16 (16-byte aligned), lse [rows] FP32, device, written.
+ *   out [rows, 512] BF16 (16-byte aligned), lse [rows] FP32, device, written
+ *   (lse may be NULL: no LSE written).
  * S in 1..4096, rows >= 1. Moving the sources between GPUs is the caller's. */
 int32_t mla_lse_merge(int32_t S, int32_t rows, const void *parts_out, const float *parts_lse,
                       void *out, float *lse, mla_stream_t stream);

@@ -159,11 +159,15 @@ class FoldedMla:
         plan_splits(self.shape, seq_lens, self.counts, self.work, stream)
 
     def decode(self, q, kv, block_table, seq_lens, bmm1_scale: float, bmm2_scale: float,
-               out=None, lse=None, stream=None):
+               out=None, lse=None, stream=None, return_lse: bool = True):
+        """out [R, M, 512] BF16 and, with return_lse, the base-2 lse [R, M]
+        (else None: the no-LSE route, nothing written for it)."""
         if out is None:
             out = torch.empty((self.R, self.M, 512), dtype=torch.bfloat16, device=self.device)
-        if lse is None:
+        if lse is None and return_lse:
             lse = torch.empty((self.R, self.M), dtype=torch.float32, device=self.device)
+        if not return_lse:
+            lse = None
         folded_decode(self.shape, q, kv, block_table, seq_lens, bmm1_scale, bmm2_scale,
                       self.counts, self.work, self.workspace, out, lse, self.status, stream)
         split_combine(self.shape, self.counts, self.work, self.workspace, bmm2_scale, out, lse,

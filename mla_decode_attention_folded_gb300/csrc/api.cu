@@ -77,11 +77,10 @@ int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
                           void* out, float* lse, int32_t* status, mla_stream_t stream) {
   int st = check_shape(shape);
   if (st != MLA_OK) return st;
-  if (!q || !kv || !block_table || !seq_lens || !counts || !work || !out || !lse)
-    return MLA_ERR_NULL;
+  if (!q || !kv || !block_table || !seq_lens || !counts || !work || !out) return MLA_ERR_NULL;
   const size_t need = workspace_bytes(*shape);
   if (need > 0 && !workspace) return MLA_ERR_NULL;
-  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(counts, 4) ||
       !aligned(work, 4) || (workspace && !aligned(workspace, 256)) ||
       (status && !aligned(status, 4)))
@@ -125,10 +124,10 @@ int32_t mla_split_combine(const mla_shape* shape, const int32_t* counts, const i
                           float bmm2_scale, void* out, float* lse, mla_stream_t stream) {
   int st = check_shape(shape);
   if (st != MLA_OK) return st;
-  if (!counts || !work || !out || !lse) return MLA_ERR_NULL;
+  if (!counts || !work || !out) return MLA_ERR_NULL;
   const size_t need = workspace_bytes(*shape);
   if (need > 0 && !workspace) return MLA_ERR_NULL;
-  if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(counts, 4) || !aligned(work, 4) ||
+  if (!aligned(out, 16) || (lse && !aligned(lse, 4)) || !aligned(counts, 4) || !aligned(work, 4) ||
       (workspace && !aligned(workspace, 256)))
     return MLA_ERR_ALIGN;
   if (list_len < plan_list_len(*shape)) return MLA_ERR_LIST;
@@ -149,9 +148,10 @@ int32_t mla_split_combine(const mla_shape* shape, const int32_t* counts, const i
 
 int32_t mla_lse_merge(int32_t S, int32_t rows, const void* parts_out, const float* parts_lse,
                       void* out, float* lse, mla_stream_t stream) {
-  if (!parts_out || !parts_lse || !out || !lse) return MLA_ERR_NULL;
+  if (!parts_out || !parts_lse || !out) return MLA_ERR_NULL;
   if (S < 1 || S > 4096 || rows < 1) return MLA_ERR_SHAPE;
-  if (!aligned(parts_out, 16) || !aligned(out, 16) || !aligned(parts_lse, 4) || !aligned(lse, 4))
+  if (!aligned(parts_out, 16) || !aligned(out, 16) || !aligned(parts_lse, 4) ||
+      (lse && !aligned(lse, 4)))
     return MLA_ERR_ALIGN;
   int st;
   if ((st = check_device()) != MLA_OK) return st;

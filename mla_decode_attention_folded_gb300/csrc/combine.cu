@@ -131,7 +131,7 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
                  ((uint32_t)f32_to_bf16_bits(acc[v].w * scale) << 16);
       *reinterpret_cast<uint2*>(dst + (v * 32 + lane) * 4) = packed;
     }
-    if (band == 0 && lane == 0)
+    if (lse && band == 0 && lane == 0)
       lse[(long long)r * M + m] = z > 0.f ? mx + __log2f(z) : -INFINITY;
   }
 }

@@ -178,7 +178,7 @@ __device__ void rows_softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* c
         if (jb.direct) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kDv + dcol);
           for (int c = 0; c < 128 * 2 / 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-          if (half == 0 && kh == 0) a.lse[orow] = -INFINITY;
+          if (a.lse && half == 0 && kh == 0) a.lse[orow] = -INFINITY;
         } else {
           uint4* dst = reinterpret_cast<uint4*>(a.part_o + orow * kDv + dcol);
           for (int c = 0; c < 128 * 4 / 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
@@ -317,7 +317,7 @@ __device__ void rows_softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* c
     tc::fence_before_sync();
     tc::mbar_arrive(&ctl->o_empty);
     if (mine && half == 0 && kh == 0) {
-      if (jb.direct) a.lse[orow] = lse2;
+      if (jb.direct && a.lse) a.lse[orow] = lse2;
       else a.part_lse[orow] = lse2;
     }
     g += jb.ntiles;

@@ -245,7 +245,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
             a.part_o[((long long)jb.item * a.M + m0 + i) * kDv + d] = 0.f;
         }
       if (gt < rows) {
-        if (jb.direct) a.lse[(long long)jb.r * a.M + m0 + gt] = -INFINITY;
+        if (jb.direct && a.lse) a.lse[(long long)jb.r * a.M + m0 + gt] = -INFINITY;
         else a.part_lse[(long long)jb.item * a.M + m0 + gt] = -INFINITY;
       }
       continue;
@@ -443,7 +443,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     tc::fence_before_sync();
     tc::mbar_arrive(&ctl->o_empty);
     if (gt < rows) {
-      if (jb.direct) a.lse[(long long)jb.r * a.M + m0 + gt] = ctl->lse[gt];
+      if (jb.direct && a.lse) a.lse[(long long)jb.r * a.M + m0 + gt] = ctl->lse[gt];
       else a.part_lse[(long long)jb.item * a.M + m0 + gt] = ctl->lse[gt];
     }
     g += jb.ntiles;

@@ -69,7 +69,7 @@ lse_merge_kernel(int S, int rows, const uint16_t* __restrict__ parts_out,
     uint4* dst = reinterpret_cast<uint4*>(out + row * kDv + lane * 16);
     dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    if (lane == 0) lse[row] = z > 0.f ? mx + __log2f(z) : -INFINITY;
+    if (lse && lane == 0) lse[row] = z > 0.f ? mx + __log2f(z) : -INFINITY;
   }
 }
 

@@ -182,6 +182,46 @@ def test_out_of_range_page_sets_status_without_fault():
     assert status & mla.FAULT_PAGE_RANGE
 
 
+def test_no_lse_route_matches_lse_route():
+    """lse = NULL (the route without an LSE): the same out, bit for bit, on
+    single- and multi-split requests and on the 32-row, 64-row and rows-as-M
+    kernels; the lse buffer a caller passed elsewhere stays untouched."""
+    for lens, k, H in (((3000, 700, 64, 0), 4, 8), ((2100, 640), 7, 8), ((1300, 90), 2, 64)):
+        b = make_batch_from_lengths(lens, k, H, seed=41, scaling="amax")
+        d = to_device(b)
+        G = _sms()
+        eng = mla.FoldedMla(b.R, b.k, b.H, d["bt"].shape[1], d["kv"].shape[0], "cuda",
+                            num_ctas=G, min_split_tokens=64)
+        bmm1, bmm2 = bmm_scales(b)
+        eng.plan(d["lens"])
+        out1, lse1 = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2)
+        sentinel = torch.full_like(lse1, 12345.0)
+        out2, lse2 = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2,
+                                return_lse=False)
+        torch.cuda.synchronize()
+        assert lse2 is None and int(eng.status.item()) == 0
+        assert torch.equal(out1.view(torch.int16), out2.view(torch.int16)), (lens, k, H)
+        assert torch.all(sentinel == 12345.0)
+        assert int((eng.counts >= 2).sum()) > 0
+        ref_o, ref_l = oracle_full(b)
+        assert_close(out2.float().reshape(b.R, b.M, 512).cpu(), lse1.cpu(), ref_o, ref_l,
+                     f"no-lse {lens}")
+
+
+def test_lse_merge_without_lse_output():
+    S, rows = 3, 70
+    g = torch.Generator().manual_seed(8)
+    parts = (torch.randn(S, rows, 512, generator=g)).to(torch.bfloat16).cuda()
+    plse = (torch.randn(S, rows, generator=g) * 4).float().cuda()
+    o1 = torch.empty(rows, 512, dtype=torch.bfloat16, device="cuda")
+    l1 = torch.empty(rows, dtype=torch.float32, device="cuda")
+    o2 = torch.empty_like(o1)
+    mla.lse_merge(parts, plse, o1, l1)
+    mla.lse_merge(parts, plse, o2, None)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
 # ---------------------------------------------------------------- combine alone
 def test_combine_on_oracle_partials():
     """mla_split_combine on partials the oracle made over the planned splits."""
