@@ -185,7 +185,7 @@ def test_out_of_range_page_sets_status_without_fault():
 def test_no_lse_route_matches_lse_route():
     """lse = NULL (the route without an LSE): the same out, bit for bit, on
     single- and multi-split requests and on the 32-row, 64-row and rows-as-M
-    kernels; the lse buffer a caller passed elsewhere stays untouched."""
+    kernels."""
     for lens, k, H in (((3000, 700, 64, 0), 4, 8), ((2100, 640), 7, 8), ((1300, 90), 2, 64)):
         b = make_batch_from_lengths(lens, k, H, seed=41, scaling="amax")
         d = to_device(b)
@@ -195,13 +195,11 @@ def test_no_lse_route_matches_lse_route():
         bmm1, bmm2 = bmm_scales(b)
         eng.plan(d["lens"])
         out1, lse1 = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2)
-        sentinel = torch.full_like(lse1, 12345.0)
         out2, lse2 = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2,
                                 return_lse=False)
         torch.cuda.synchronize()
         assert lse2 is None and int(eng.status.item()) == 0
         assert torch.equal(out1.view(torch.int16), out2.view(torch.int16)), (lens, k, H)
-        assert torch.all(sentinel == 12345.0)
         assert int((eng.counts >= 2).sum()) > 0
         ref_o, ref_l = oracle_full(b)
         assert_close(out2.float().reshape(b.R, b.M, 512).cpu(), lse1.cpu(), ref_o, ref_l,
