@@ -18,6 +18,8 @@ What it computes, from the pages' problem statement:
 * ``merge``     -- the LSE merge of split partials (drafter-attention page,
                    ``DraftDcp``: exp2(lse - max) / sum in FP32 on the pages,
                    float64 here).
+* ``uv``        -- the W_UV up-projection of each head's merged latent row
+                   (drafter-attention page, ``DraftDcp`` and ``latent_major``).
 * ``planner``   -- the integer split planner (balanced and uniform) that the
                    device planner must reproduce bit for bit. The pages name
                    the idea (balanced-MLA page, module overview; rank rule of

@@ -24,7 +24,9 @@ Recipe (stated once, used everywhere):
 * pages: one random permutation of [0, total pages) handed out to the
   requests in order; block-table entries past a request's pages hold
   ``fill`` (0 for timing runs, an out-of-range sentinel in bounds tests);
-* softmax scale 1/sqrt(192) (qk_nope 128 + rope 64) for every workload.
+* softmax scale 1/sqrt(192) (qk_nope 128 + rope 64) for every workload;
+* W_UV (the up-projection after the merge): N(0, 1) / sqrt(512) per element,
+  rounded to BF16, seeded per use (``make_w_uv``).
 """
 from __future__ import annotations
 
@@ -196,3 +198,12 @@ def shard_pages(batch: Batch, shards: int, shard: int) -> Batch:
     return Batch(q=batch.q, kv=batch.kv, block_table=torch.from_numpy(lbt),
                  seq_lens=torch.from_numpy(llen), k=batch.k, H=batch.H,
                  q_scale=batch.q_scale, kv_scale=batch.kv_scale, sm_scale=batch.sm_scale)
+
+
+def make_w_uv(H: int, seed: int) -> torch.Tensor:
+    """Synthetic per-head W_UV [H, 512, 128] as BF16 (no trained weights exist
+    here): N(0, 1) / sqrt(512) drawn in float32, rounded to BF16 by PyTorch's
+    cast, so each output has about unit variance for unit-variance inputs."""
+    gen = torch.Generator().manual_seed(seed)
+    w = torch.randn((H, D_V, 128), generator=gen, dtype=torch.float32) / math.sqrt(D_V)
+    return w.to(torch.bfloat16)
