@@ -309,6 +309,33 @@ class Runner:
         self.decode()
         self.combine()
 
+    # The W_UV leg: the decode without an LSE, then the split reduction fused
+    # with the up-projection (synthetic BF16 weights).
+    def uv_setup(self, dev):
+        from workloads import make_w_uv
+        b = self.b
+        self.w_uv = make_w_uv(b.H, seed=2024).transpose(1, 2).contiguous().to(dev)
+        self.y = torch.empty((b.R * b.k, b.H, 128), dtype=torch.bfloat16, device=dev)
+
+    def decode_nolse(self):
+        e = self.eng
+        self.mla.folded_decode(e.shape, self.q, self.kv, self.bt, self.lens, self.bmm1,
+                               self.bmm2, e.counts, e.work, e.workspace, self.out, None,
+                               e.status)
+
+    def uv(self):
+        e = self.eng
+        self.mla.uv_combine(e.shape, e.counts, e.work, e.workspace, self.bmm2, self.out,
+                            self.w_uv, self.y, e.status)
+
+    def uv_times(self, steps, flush):
+        """(plan -> decode -> fused W_UV reduction) per step, and the fused
+        reduction alone after an untimed plan + decode."""
+        chain = self.graph(lambda: (self.plan(), self.decode_nolse(), self.uv()))
+        gpd = self.graph(lambda: (self.plan(), self.decode_nolse()))
+        guv = self.graph(self.uv)
+        return self._time(chain, steps, flush), self._time(guv, steps, flush, before=gpd)
+
     def graph(self, fn):
         """fn's launches captured once into a CUDA graph (replayed per step, so
         host launch overhead stays out of the timed region)."""
@@ -458,6 +485,8 @@ def run_ours(args):
     step_ms = main.timed(args.steps, max(args.warmup, 3), flush, barrier)
     clk = clocks.stop()
     plan_ms, dec_ms, comb_ms = main.kernel_times(min(args.steps, 1000), flush)
+    main.uv_setup(dev)
+    uv_step_ms, uv_ms = main.uv_times(min(args.steps, 1000), flush)
     no_plan_ms, no_comb_ms = main.marginal_times(min(args.steps, 1000), flush)
     status = int(main.eng.status.item())
     step_ms, dec_ms = max_over_ranks([step_ms, dec_ms], dev)
@@ -521,6 +550,11 @@ def run_ours(args):
         "kernel_ms": {"plan": plan_ms, "decode": dec_ms, "combine": comb_ms},
         "chain_ms": {"step": step_ms, "without_plan": no_plan_ms, "without_combine": no_comb_ms},
         "variants": variants,
+        "w_uv": {"step_ms": uv_step_ms, "rows_per_s": world * rows / (uv_step_ms / 1e3),
+                 "uv_kernel_ms": uv_ms,
+                 "what": "plan -> decode (no LSE) -> split reduction fused with the W_UV "
+                         "up-projection to [R*k, H, 128] BF16 (synthetic BF16 W_UV)",
+                 "gemm_flops": 2 * batch.R * batch.k * batch.H * 512 * 128},
         "roofline": dict(roof, traffic=profiled_traffic(args.workload),
                          kernel="mla_folded_decode", algorithmic_bytes_per_launch=algo,
                          algorithmic_flops_per_launch=flops,

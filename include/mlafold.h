@@ -170,6 +170,31 @@ int32_t mla_split_combine(const mla_shape *shape, const int32_t *counts, const i
                           int32_t list_len, const void *workspace, size_t workspace_bytes,
                           float bmm2_scale, void *out, float *lse, mla_stream_t stream);
 
+/* The split reduction fused with the W_UV up-projection (drafter-attention
+ * page, `DraftDcp`: the head owner merges its heads' partial rows by
+ * exp2(lse - max) / sum in FP32 with one BF16 rounding and applies W_UV as a
+ * BF16 MMA with FP32 accumulation; `latent_major` for the weight layout):
+ *   y[t, h, :] = bf16( bf16(o(t, h)) . W_UV[h] ),   W_UV[h] is [512, 128],
+ * where o(t, h) is the merged 512-dim row of token t (of R*k, token-major) and
+ * head h, as mla_split_combine would write it: from the split partials in the
+ * workspace for a request with two or more splits, else the row `out` already
+ * holds. The merged rows themselves are not written anywhere.
+ *   counts, work, list_len, workspace, workspace_bytes, bmm2_scale: the plan,
+ *               workspace and scale of the mla_folded_decode call before it.
+ *   out   [R, k*H, 512] BF16, device, 16-byte aligned: that decode's output
+ *         (read for one-split requests only).
+ *   w_uv  [H, 128, 512] BF16, device, 16-byte aligned: W_UV[h] transposed, row j
+ *         holding W_UV[h, :, j] (latent-contiguous).
+ *   y     [R*k, H, 128] BF16, device, 16-byte aligned, written.
+ *   status optional int32 device word: MLA_FAULT_* bits (a malformed plan, a
+ *         wait that timed out), as for mla_folded_decode.
+ * The pages run this step after the DCP exchange; here it follows the
+ * single-GPU decode. */
+int32_t mla_uv_combine(const mla_shape *shape, const int32_t *counts, const int32_t *work,
+                       int32_t list_len, const void *workspace, size_t workspace_bytes,
+                       float bmm2_scale, const void *out, const void *w_uv, void *y,
+                       int32_t *status, mla_stream_t stream);
+
 /* Merge of S partial results of the same rows over disjoint key sets, e.g.
  * the S shards of a decode-context-parallel KV cache each decoded on its own
  * (drafter-attention page, `DraftDcp`: each head's rows are merged over the

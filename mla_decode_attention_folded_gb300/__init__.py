@@ -28,7 +28,7 @@ from ._lib import (FAULT_PAGE_RANGE, FAULT_WAIT_TIMEOUT, FAULT_WORK_ITEM, MlaErr
 
 __all__ = ["MlaShape", "MlaError", "POLICY_BALANCED", "POLICY_UNIFORM", "make_shape",
            "plan_list_len", "workspace_bytes", "plan_splits", "folded_decode",
-           "split_combine", "lse_merge", "folded_decode_noalloc", "FoldedMla", "fold_factor", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
+           "split_combine", "uv_combine", "lse_merge", "folded_decode_noalloc", "FoldedMla", "fold_factor", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
            "FAULT_WORK_ITEM", "library_path"]
 
 PAGE = 64
@@ -105,6 +105,17 @@ def split_combine(shape: MlaShape, counts, work, workspace, bmm2_scale: float, o
         float(bmm2_scale), _ptr(out), _ptr(lse), _stream(stream)))
 
 
+def uv_combine(shape: MlaShape, counts, work, workspace, bmm2_scale: float, out, w_uv, y,
+               status=None, stream=None) -> None:
+    """The split reduction fused with the W_UV up-projection: y [R*k, H, 128]
+    BF16 from the decode's workspace partials and one-split rows `out`, with
+    w_uv [H, 128, 512] BF16 (W_UV[h] transposed, latent-contiguous)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.check("mla_uv_combine", _lib.load().mla_uv_combine(
+        ctypes.byref(shape), _ptr(counts), _ptr(work), work.numel(), _ptr(workspace), ws_bytes,
+        float(bmm2_scale), _ptr(out), _ptr(w_uv), _ptr(y), _ptr(status), _stream(stream)))
+
+
 def lse_merge(parts_out, parts_lse, out, lse, stream=None) -> None:
     """Merge S partial results over disjoint key sets: parts_out [S, rows, 512]
     BF16 and parts_lse [S, rows] FP32 log2 -> out [rows, 512], lse [rows]
@@ -173,3 +184,19 @@ class FoldedMla:
         split_combine(self.shape, self.counts, self.work, self.workspace, bmm2_scale, out, lse,
                       stream)
         return out, lse
+
+    def decode_uv(self, q, kv, block_table, seq_lens, bmm1_scale: float, bmm2_scale: float,
+                  w_uv, y=None, out=None, stream=None):
+        """The decode followed by the split reduction fused with W_UV:
+        y [R*k, H, 128] BF16 (w_uv [H, 128, 512] BF16, latent-contiguous).
+        `out` receives the one-split requests' rows only; no LSE is written."""
+        if out is None:
+            out = torch.empty((self.R, self.M, 512), dtype=torch.bfloat16, device=self.device)
+        if y is None:
+            y = torch.empty((self.R * self.k, self.H, 128), dtype=torch.bfloat16,
+                            device=self.device)
+        folded_decode(self.shape, q, kv, block_table, seq_lens, bmm1_scale, bmm2_scale,
+                      self.counts, self.work, self.workspace, out, None, self.status, stream)
+        uv_combine(self.shape, self.counts, self.work, self.workspace, bmm2_scale, out, w_uv, y,
+                   self.status, stream)
+        return y

@@ -21,7 +21,7 @@ FAULT_WAIT_TIMEOUT, FAULT_PAGE_RANGE, FAULT_WORK_ITEM = 0x1, 0x2, 0x4
 # Every symbol include/mlafold.h declares.
 EXPORTS = ("mla_plan_list_len", "mla_workspace_bytes", "mla_plan_splits",
            "mla_folded_decode", "mla_split_combine", "mla_lse_merge",
-           "mla_folded_decode_noalloc")
+           "mla_folded_decode_noalloc", "mla_uv_combine")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -66,6 +66,8 @@ def load() -> ctypes.CDLL:
     lib.mla_lse_merge.restype = I32
     lib.mla_folded_decode_noalloc.argtypes = [SP, P, P, P, P, F, F, P, P, I32, P, P, P, P]
     lib.mla_folded_decode_noalloc.restype = I32
+    lib.mla_uv_combine.argtypes = [SP, P, P, I32, P, SZ, F, P, P, P, P, P]
+    lib.mla_uv_combine.restype = I32
     _lib = lib
     return lib
 

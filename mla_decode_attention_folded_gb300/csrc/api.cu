@@ -146,6 +146,36 @@ int32_t mla_split_combine(const mla_shape* shape, const int32_t* counts, const i
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+int32_t mla_uv_combine(const mla_shape* shape, const int32_t* counts, const int32_t* work,
+                       int32_t list_len, const void* workspace, size_t workspace_bytes_given,
+                       float bmm2_scale, const void* out, const void* w_uv, void* y,
+                       int32_t* status, mla_stream_t stream) {
+  int st = check_shape(shape);
+  if (st != MLA_OK) return st;
+  if (!counts || !work || !out || !w_uv || !y) return MLA_ERR_NULL;
+  const size_t need = workspace_bytes(*shape);
+  if (need > 0 && !workspace) return MLA_ERR_NULL;
+  if (!aligned(out, 16) || !aligned(w_uv, 16) || !aligned(y, 16) || !aligned(counts, 4) ||
+      !aligned(work, 4) || (workspace && !aligned(workspace, 256)) ||
+      (status && !aligned(status, 4)))
+    return MLA_ERR_ALIGN;
+  if (list_len < plan_list_len(*shape)) return MLA_ERR_LIST;
+  if (workspace_bytes_given < need) return MLA_ERR_WORKSPACE;
+  if (!std::isfinite(bmm2_scale)) return MLA_ERR_SHAPE;
+  if ((st = check_device()) != MLA_OK) return st;
+  const int M = group_rows(*shape);
+  const int slots = partial_slots(*shape);
+  const float* po = static_cast<const float*>(workspace);
+  const float* pl = workspace ? reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
+                                                               partial_out_bytes(slots, M))
+                              : nullptr;
+  cudaError_t e = launch_uv(*shape, counts, work, list_len, po, pl, slots, bmm2_scale,
+                            static_cast<const uint16_t*>(out), static_cast<const uint16_t*>(w_uv),
+                            static_cast<uint16_t*>(y), status,
+                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int32_t mla_lse_merge(int32_t S, int32_t rows, const void* parts_out, const float* parts_lse,
                       void* out, float* lse, mla_stream_t stream) {
   if (!parts_out || !parts_lse || !out) return MLA_ERR_NULL;

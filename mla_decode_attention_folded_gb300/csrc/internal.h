@@ -108,6 +108,10 @@ cudaError_t launch_combine(const mla_shape& s, const int32_t* counts, const int3
                            float bmm2, uint16_t* out, float* lse, cudaStream_t st);
 cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_rows(const mla_shape& s, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_uv(const mla_shape& s, const int32_t* counts, const int32_t* work,
+                      int list_len, const float* part_o, const float* part_lse, int slots,
+                      float bmm2, const uint16_t* out, const uint16_t* w_uv, uint16_t* y,
+                      int32_t* status, cudaStream_t st);
 cudaError_t launch_lse_merge(int S, int rows, const uint16_t* parts_out, const float* parts_lse,
                              uint16_t* out, float* lse, cudaStream_t st);
 
