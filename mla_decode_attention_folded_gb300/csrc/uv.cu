@@ -6,16 +6,17 @@
 // rounding and applies W_UV as a BF16 MMA; `latent_major`: W_UV stored
 // latent-contiguous). The merged 512-dim rows never reach HBM.
 //
-// One CTA per (32-token block, head). The 128 W_UV output dims are the MMA's
-// M and the 32 tokens its N ("swap-AB": 32 tokens keep even the smallest
-// batches spread over many SMs):
+// Persistent CTAs walk contiguous ranges of (head, 32-token block) tiles,
+// head-major. The 128 W_UV output dims are the MMA's M and the 32 tokens its
+// N ("swap-AB": 32 tokens keep even the smallest batches spread over SMs):
 //     Y^T[128, 32] = W_UV[h]^T[128, 512] . X[32, 512]^T,  8 chunks x 4 MMAs (K = 16)
-// X, the CTA's 32 merged BF16 rows, is built in shared memory by 256 reducer
-// threads (8 per token row, 64 latent dims each): from the decode's own BF16
+// W_UV[h] (128 KB) stays in shared memory while the CTA's tiles share a head.
+// X, a tile's 32 merged BF16 rows, is built in shared memory by 256 reducer
+// threads (8 per token row, interleaved 16-byte pieces): from the decode's own BF16
 // row for a request with one split, else from the FP32 split partials and
-// their LSEs. W_UV[h]'s eight 64-dim chunks stream in by TMA through two
-// stages. The accumulator lives in 32 TMEM columns; four warps read it back
-// and store Y.
+// their LSEs. X and the TMEM accumulator are double-buffered, so a tile's
+// reduction overlaps the previous tile's MMAs and the read-back of the one
+// before; four of the reducer warps read the accumulator back and store Y.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -26,27 +27,32 @@
 namespace mlafold {
 namespace {
 
-constexpr int kTok = 32;                       // tokens per CTA: the MMA's N
+constexpr int kTok = 32;                       // tokens per tile: the MMA's N
 constexpr int kOut = 128;                      // W_UV output dims: the MMA's M
 constexpr int kChunks = kDv / 64;              // 64 latent dims = 128 B of BF16 per chunk
 constexpr int kRed = 256;                      // reducer threads: 8 per token row
 constexpr int kThreads = 32 + kRed;            // warp 0: TMA + MMA + TMEM owner
-constexpr int kWStage = kOut * 128;            // one W chunk: 128 rows x 128 B
+constexpr int kWChunk = kOut * 128;            // one W chunk: 128 rows x 128 B
 constexpr int kXChunk = kTok * 128;            // one X chunk: 32 rows x 128 B
-constexpr int kOffW = 0;                       // two W stages
-constexpr int kOffX = 2 * kWStage;             // X, eight chunks
-constexpr int kOffStart = kOffX + kChunks * kXChunk;   // first slot of each multi-split row
+constexpr int kXBytes = kChunks * kXChunk;     // one X buffer
+constexpr int kOffW = 0;                       // W_UV[h], eight chunks
+constexpr int kOffX = kChunks * kWChunk;       // two X buffers
+constexpr int kOffStart = kOffX + 2 * kXBytes; // first slot of each multi-split row group
 constexpr int kOffBar = kOffStart + kMaxR * 4;
-constexpr int kSmemBytes = kOffBar + 128 + 1024;        // + control block, + alignment slack
+constexpr int kSmemBytes = kOffBar + 256 + 1024;        // + control block, + alignment slack
+constexpr uint32_t kTmemCols = 2 * kTok;       // two FP32 accumulators of 32 columns
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kOut, kTok);
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 static_assert(kOffX % 1024 == 0 && kXChunk % 1024 == 0, "swizzle atoms need 1 KB alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 struct UvCtl {
-  uint64_t w_full[2];   // TMA -> MMA: W chunk landed
-  uint64_t w_free[2];   // MMA -> TMA: the chunk's MMAs finished reading the stage
-  uint64_t x_full;      // reducers -> MMA: X written
-  uint64_t d_full;      // MMA -> epilogue: accumulator final
+  uint64_t w_full[kChunks];   // TMA -> MMA: W chunk landed (one phase per head loaded)
+  uint64_t x_full[2];         // reducers -> MMA: X buffer written
+  uint64_t x_empty[2];        // MMA -> reducers (and W reload): the tile's MMAs finished
+  uint64_t d_full[2];         // MMA -> read-back: accumulator final
+  uint64_t d_empty[2];        // read-back -> MMA: accumulator read
+  uint64_t drain;             // MMA issuer, on abort: every MMA it issued has finished
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -78,16 +84,23 @@ __device__ __forceinline__ bool uv_wait(uint64_t* bar, uint32_t parity, UvCtl* c
   }
 }
 
-// X chunk c, row `row`, is K-major with the 128-byte swizzle: its 16-byte
-// piece p lives at ((p ^ (row & 7)) * 16) of the row's 128 bytes.
-__device__ __forceinline__ void put_piece(uint8_t* xrow, int row, int p, uint4 v) {
-  *reinterpret_cast<uint4*>(xrow + ((p ^ (row & 7)) * 16)) = v;
+// X is K-major with the 128-byte swizzle: 64 latent dims (128 B of BF16) per
+// chunk, 16-byte piece p of a row at ((p ^ (row & 7)) * 16) within the row.
+// Byte offset in X of BF16 latent dims [8 i, 8 i + 8) of token row `row`:
+__device__ __forceinline__ int x_piece(int row, int i) {
+  return (i >> 3) * kXChunk + row * 128 + (((i & 7) ^ (row & 7)) << 4);
 }
 
-// Writes the BF16 values [64 c, 64 c + 64) of one token row's merged output
-// into its row of X chunk c.
-__device__ __forceinline__ void merged_chunk(const UvArgs& a, const int* s_start, int tau, int h,
-                                             int c, uint8_t* xrow, int row) {
+// Writes one token row's merged BF16 latent output into X. The 8 threads of the
+// row (consecutive lanes; this one is `c`) cover it interleaved: thread c takes
+// the 16-byte pieces 8 v + c (v = 0..7) of the BF16 row, or the float4s
+// 8 v + c (v = 0..15) of an FP32 partial row, so that each warp-wide load
+// reads whole 128-byte lines.
+// `ready()` is called once, after the row's global loads and before its first
+// shared-memory write (it waits for the X buffer to be free); false = give up.
+template <typename Ready>
+__device__ __forceinline__ bool merged_row(const UvArgs& a, const int* s_start, int tau, int h,
+                                           int c, uint8_t* x, int row, Ready ready) {
   const uint4 zero = make_uint4(0, 0, 0, 0);
   int n = 0, r = 0, t = 0, i = 0, mg = 0;
   if (tau < a.T) {
@@ -99,64 +112,88 @@ __device__ __forceinline__ void merged_chunk(const UvArgs& a, const int* s_start
     n = a.counts[i];
   }
   if (tau >= a.T) {                             // rows past the batch stay zero
+    if (!ready()) return false;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) put_piece(xrow, row, p, zero);
-    return;
+    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(x + x_piece(row, 8 * v + c)) = zero;
+    return true;
   }
   if (n <= 1) {                                 // one split: the decode's BF16 row
     const uint4* src = reinterpret_cast<const uint4*>(
-        a.out + ((size_t)r * a.M + (size_t)t * a.H + h) * kDv + c * 64);
-    uint4 v[8];
+        a.out + ((size_t)r * a.M + (size_t)t * a.H + h) * kDv);
+    uint4 v8[8];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) v[p] = src[p];
+    for (int v = 0; v < 8; ++v) v8[v] = src[8 * v + c];
+    if (!ready()) return false;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) put_piece(xrow, row, p, v[p]);
-    return;
+    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(x + x_piece(row, 8 * v + c)) = v8[v];
+    return true;
   }
   const int start = s_start[i];
   if (start < 0 || start + n > a.slots) {       // not a plan of this shape: leave zeros
     if (a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
+    if (!ready()) return false;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) put_piece(xrow, row, p, zero);
-    return;
+    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(x + x_piece(row, 8 * v + c)) = zero;
+    return true;
   }
+  // LSEs of 8 splits at a time, one per thread of the row: max and weights by
+  // shuffles within the 8.
+  const unsigned grp = 0xFFu << (threadIdx.x & 24);
+  const int base = threadIdx.x & 24;
   const float* lse = a.part_lse + (size_t)start * a.Mg + mg;
   float mx = -INFINITY;
-  for (int s = 0; s < n; ++s) mx = fmaxf(mx, lse[(size_t)s * a.Mg]);
-  const float* po = a.part_o + ((size_t)start * a.Mg + mg) * kDv + c * 64;
-  const size_t stride = (size_t)a.Mg * kDv;
+  for (int g0 = 0; g0 < n; g0 += 8)
+    if (g0 + c < n) mx = fmaxf(mx, lse[(size_t)(g0 + c) * a.Mg]);
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(grp, mx, o));
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + ((size_t)start * a.Mg + mg) * kDv);
+  const size_t stride = (size_t)a.Mg * kDv / 4;  // float4s between splits
   float4 acc[16];
 #pragma unroll
   for (int v = 0; v < 16; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   float z = 0.f;
-  for (int s = 0; s < n; ++s) {
-    const float4* src = reinterpret_cast<const float4*>(po + s * stride);
-    float4 x[16];
+  for (int g0 = 0; g0 < n; g0 += 8) {
+    const float l = g0 + c < n ? lse[(size_t)(g0 + c) * a.Mg] : -INFINITY;
+    const float wc = (mx == -INFINITY || l == -INFINITY) ? 0.f : ex2(l - mx);
+    z += wc;
+    const int m = min(8, n - g0);
+    // Two splits' partial rows in flight per round trip.
+    for (int u = 0; u < m; u += 2) {
+      const bool two = u + 1 < m;
+      const float w0 = __shfl_sync(grp, wc, base + u);
+      const float w1 = __shfl_sync(grp, wc, base + (two ? u + 1 : u));
+      const float4* s0 = po + (size_t)(g0 + u) * stride;
+      const float4* s1 = po + (size_t)(g0 + (two ? u + 1 : u)) * stride;
+      float4 x0[16], x1[16];                   // x1 repeats x0 (weight 0) when m is odd
 #pragma unroll
-    for (int v = 0; v < 16; ++v) x[v] = src[v];
-    const float l = lse[(size_t)s * a.Mg];
-    const float w = (mx == -INFINITY || l == -INFINITY) ? 0.f : ex2(l - mx);
-    z += w;
+      for (int v = 0; v < 16; ++v) {
+        x0[v] = s0[8 * v + c];
+        x1[v] = s1[8 * v + c];
+      }
+      const float v1 = two ? w1 : 0.f;
 #pragma unroll
-    for (int v = 0; v < 16; ++v) {
-      acc[v].x += w * x[v].x; acc[v].y += w * x[v].y;
-      acc[v].z += w * x[v].z; acc[v].w += w * x[v].w;
+      for (int v = 0; v < 16; ++v) {
+        acc[v].x += w0 * x0[v].x + v1 * x1[v].x; acc[v].y += w0 * x0[v].y + v1 * x1[v].y;
+        acc[v].z += w0 * x0[v].z + v1 * x1[v].z; acc[v].w += w0 * x0[v].w + v1 * x1[v].w;
+      }
     }
   }
-  const float sc = z > 0.f ? a.bmm2 / z : 0.f;
 #pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const float4 u = acc[2 * p], w = acc[2 * p + 1];
-    put_piece(xrow, row, p,
-              make_uint4((uint32_t)f32_to_bf16_bits(u.x * sc) |
-                             ((uint32_t)f32_to_bf16_bits(u.y * sc) << 16),
-                         (uint32_t)f32_to_bf16_bits(u.z * sc) |
-                             ((uint32_t)f32_to_bf16_bits(u.w * sc) << 16),
-                         (uint32_t)f32_to_bf16_bits(w.x * sc) |
-                             ((uint32_t)f32_to_bf16_bits(w.y * sc) << 16),
-                         (uint32_t)f32_to_bf16_bits(w.z * sc) |
-                             ((uint32_t)f32_to_bf16_bits(w.w * sc) << 16)));
+  for (int o = 1; o < 8; o <<= 1) z += __shfl_xor_sync(grp, z, o);
+  const float sc = z > 0.f ? a.bmm2 / z : 0.f;
+  // float4 8 v + c holds latent dims 4 (8 v + c) ..: half (c & 1) of the 16-byte
+  // BF16 piece 4 v + c / 2.
+  if (!ready()) return false;
+#pragma unroll
+  for (int v = 0; v < 16; ++v) {
+    const float4 u = acc[v];
+    const uint2 b = make_uint2((uint32_t)f32_to_bf16_bits(u.x * sc) |
+                                   ((uint32_t)f32_to_bf16_bits(u.y * sc) << 16),
+                               (uint32_t)f32_to_bf16_bits(u.z * sc) |
+                                   ((uint32_t)f32_to_bf16_bits(u.w * sc) << 16));
+    *reinterpret_cast<uint2*>(x + x_piece(row, 4 * v + (c >> 1)) + (c & 1) * 8) = b;
   }
+  return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -167,21 +204,27 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
   UvCtl* ctl = reinterpret_cast<UvCtl*>(smem + kOffBar);
   int* s_start = reinterpret_cast<int*>(smem + kOffStart);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y, tok0 = blockIdx.x * kTok;
+  // This CTA's tiles: a contiguous, head-major range of (head, token block).
+  const int nblk = (int)cdiv(a.T, kTok);
+  const long long ntiles = (long long)nblk * a.H;
+  const int t_begin = (int)(ntiles * blockIdx.x / gridDim.x);
+  const int t_end = (int)(ntiles * (blockIdx.x + 1) / gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&ctl->w_full[s], 1);
-      tc::mbar_init(&ctl->w_free[s], 1);
+    for (int c = 0; c < kChunks; ++c) tc::mbar_init(&ctl->w_full[c], 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl->x_full[b], kRed);
+      tc::mbar_init(&ctl->x_empty[b], 1);
+      tc::mbar_init(&ctl->d_full[b], 1);
+      tc::mbar_init(&ctl->d_empty[b], 128);
     }
-    tc::mbar_init(&ctl->x_full, kRed);
-    tc::mbar_init(&ctl->d_full, 1);
+    tc::mbar_init(&ctl->drain, 1);
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
   }
   if (warp == 0) {
     if (lane == 0) tc::prefetch_tmap(&tm_w);
-    tc::tmem_alloc(&ctl->tmem_base, 32);
+    tc::tmem_alloc(&ctl->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
   for (int i = threadIdx.x; i < a.plan_rows; i += blockDim.x) s_start[i] = -1;
@@ -208,72 +251,108 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      int last_parity[2] = {-1, -1};
-      auto load_w = [&](int c) {
-        const int st = c & 1;
-        tc::mbar_arrive_expect_tx(&ctl->w_full[st], kWStage);
-        tc::tma_load_2d(smem + kOffW + st * kWStage, &tm_w, &ctl->w_full[st], c * 128, h * kOut);
-        last_parity[st] = (c >> 1) & 1;
-      };
-      load_w(0);
-      load_w(1);
-      ok = uv_wait(&ctl->x_full, 0, ctl, a.status);
-      for (int c = 0; ok && c < kChunks; ++c) {
-        const int st = c & 1;
-        if (!(ok = uv_wait(&ctl->w_full[st], (c >> 1) & 1, ctl, a.status))) break;
-        tc::fence_after_sync();
-        const uint32_t wa = tc::smem_u32(smem + kOffW + st * kWStage);
-        const uint32_t xa = tc::smem_u32(smem + kOffX + c * kXChunk);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tmem, tc::smem_desc(wa + kk * 32, 16, 1024, tc::kSw128),
-                       tc::smem_desc(xa + kk * 32, 16, 1024, tc::kSw128), kIdesc, (c | kk) != 0);
-        tc::mma_commit(&ctl->w_free[st]);
-        if (c + 2 < kChunks) {
-          if (!(ok = uv_wait(&ctl->w_free[st], (c >> 1) & 1, ctl, a.status))) break;
-          load_w(c + 2);
-        }
-      }
-      tc::mma_commit(&ctl->d_full);            // once every MMA above has finished
-      if (!ok) {                               // never leave with copies in flight
-        const unsigned long long t0 = tc::globaltimer_ns();
-        for (int st = 0; st < 2; ++st)
-          while (last_parity[st] >= 0 && !tc::mbar_try_wait(&ctl->w_full[st], last_parity[st]) &&
-                 tc::globaltimer_ns() - t0 < kTimeoutNs) {
+      int cur_h = -1, loads = 0;
+      bool w_ready = false;
+      int it = 0;
+      for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
+        const int h = tile / nblk, buf = it & 1;
+        if (h != cur_h) {
+          // The previous tile's MMAs must be done reading W before it is replaced.
+          if (it > 0 &&
+              !(ok = uv_wait(&ctl->x_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, ctl, a.status)))
+            break;
+          for (int c = 0; c < kChunks; ++c) {
+            tc::mbar_arrive_expect_tx(&ctl->w_full[c], kWChunk);
+            tc::tma_load_2d(smem + kOffW + c * kWChunk, &tm_w, &ctl->w_full[c], c * 128,
+                            h * kOut);
           }
-        while (!tc::mbar_try_wait(&ctl->d_full, 0) && tc::globaltimer_ns() - t0 < kTimeoutNs) {
+          ++loads;
+          cur_h = h;
+          w_ready = false;
+        }
+        if (!(ok = uv_wait(&ctl->x_full[buf], (it >> 1) & 1, ctl, a.status))) break;
+        if (it >= 2 &&
+            !(ok = uv_wait(&ctl->d_empty[buf], ((it - 2) >> 1) & 1, ctl, a.status)))
+          break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + buf * kTok;
+        for (int c = 0; ok && c < kChunks; ++c) {
+          if (!w_ready && !(ok = uv_wait(&ctl->w_full[c], (loads - 1) & 1, ctl, a.status))) break;
+          tc::fence_after_sync();
+          const uint32_t wa = tc::smem_u32(smem + kOffW + c * kWChunk);
+          const uint32_t xa = tc::smem_u32(smem + kOffX + buf * kXBytes + c * kXChunk);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(d, tc::smem_desc(wa + kk * 32, 16, 1024, tc::kSw128),
+                         tc::smem_desc(xa + kk * 32, 16, 1024, tc::kSw128), kIdesc,
+                         (c | kk) != 0);
+        }
+        if (!ok) break;
+        w_ready = true;
+        tc::mma_commit(&ctl->x_empty[buf]);
+        tc::mma_commit(&ctl->d_full[buf]);
+      }
+      if (!ok) {                               // never leave with copies or MMAs in flight
+        tc::mma_commit(&ctl->drain);
+        const unsigned long long t0 = tc::globaltimer_ns();
+        if (loads > 0)
+          for (int c = 0; c < kChunks; ++c)
+            while (!tc::mbar_try_wait(&ctl->w_full[c], (loads - 1) & 1) &&
+                   tc::globaltimer_ns() - t0 < kTimeoutNs) {
+            }
+        while (!tc::mbar_try_wait(&ctl->drain, 0) && tc::globaltimer_ns() - t0 < kTimeoutNs) {
         }
       }
     }
   } else {
     const int rt = threadIdx.x - 32;
-    const int row = rt >> 3, c = rt & 7;        // token row of the tile, its 64-dim chunk
-    merged_chunk(a, s_start, tok0 + row, h, c, smem + kOffX + c * kXChunk + row * 128, row);
-    tc::fence_proxy_async_smem();
-    tc::mbar_arrive(&ctl->x_full);
-
-    if (warp <= 4) {                            // four warps: one TMEM lane quarter each
-      const bool ok = uv_wait(&ctl->d_full, 0, ctl, a.status);
+    const int row = rt >> 3, c = rt & 7;        // token row of a tile, this thread's eighth
+    const bool reads_back = warp <= 4;          // four warps: one TMEM lane quarter each
+    const int q = warp & 3;
+    bool ok = true;
+    auto read_back = [&](int tile, int it) {
+      const int h = tile / nblk, tok0 = (tile % nblk) * kTok, buf = it & 1;
+      if (!(ok = uv_wait(&ctl->d_full[buf], (it >> 1) & 1, ctl, a.status))) return;
       tc::fence_after_sync();
-      const int q = warp & 3;
-      const int j = q * 32 + lane;              // output dim = accumulator row = TMEM lane
       uint32_t raw[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16), raw);
+      tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * kTok, raw);
       tc::tmem_wait_ld();
-      if (ok && !*reinterpret_cast<volatile int*>(&ctl->abort_flag)) {
+      tc::fence_before_sync();
+      tc::mbar_arrive(&ctl->d_empty[buf]);
+      const int j = q * 32 + lane;              // output dim = accumulator row = TMEM lane
 #pragma unroll
-        for (int col = 0; col < kTok; ++col) {
-          const int tau = tok0 + col;
-          if (tau < a.T)
-            a.y[((size_t)tau * a.H + h) * kOut + j] = f32_to_bf16_bits(__uint_as_float(raw[col]));
-        }
+      for (int col = 0; col < kTok; ++col) {
+        const int tau = tok0 + col;
+        if (tau < a.T)
+          a.y[((size_t)tau * a.H + h) * kOut + j] = f32_to_bf16_bits(__uint_as_float(raw[col]));
+      }
+    };
+    int it = 0;
+    for (int tile = t_begin; tile < t_end; ++tile, ++it) {
+      const int h = tile / nblk, tok0 = (tile % nblk) * kTok, buf = it & 1;
+      // X[buf] is free once the MMAs of the tile two back have read it: wait
+      // for that only after the row's loads are in flight.
+      const int it_now = it;
+      auto x_free = [&]() {
+        return it_now < 2 ||
+               uv_wait(&ctl->x_empty[it_now & 1], ((it_now - 2) >> 1) & 1, ctl, a.status);
+      };
+      if (!(ok = merged_row(a, s_start, tok0 + row, h, c, smem + kOffX + buf * kXBytes, row,
+                            x_free)))
+        break;
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&ctl->x_full[buf]);
+      if (reads_back && it > 0) {
+        read_back(tile - 1, it - 1);
+        if (!ok) break;
       }
     }
+    if (ok && reads_back && it > 0) read_back(t_end - 1, it - 1);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 32);
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 uv_encode_fn() {
@@ -334,7 +413,8 @@ cudaError_t launch_uv(const mla_shape& s, const int32_t* counts, const int32_t* 
   a.Mg = group_rows(s);
   a.T = s.R * s.k;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)cdiv(a.T, kTok), (unsigned)s.H);
+  const long long ntiles = cdiv(a.T, kTok) * (long long)s.H;
+  cfg.gridDim = dim3((unsigned)(ntiles < s.num_ctas ? ntiles : s.num_ctas));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
