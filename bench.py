@@ -526,10 +526,10 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rps, rows, el, chunks = OracleSampler(batch).run(args.cpu_seconds)
+        rps, cpu_rows, el, chunks = OracleSampler(batch).run(args.cpu_seconds)
         cpu = {"value": rps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                "sample": f"{chunks} consecutive {OracleSampler.CHUNK}-key chunks of the "
-                         f"requests of {args.workload} = {rows:.1f} query-token rows (the batch "
+                         f"requests of {args.workload} = {cpu_rows:.1f} query-token rows (the batch "
                          f"has {batch.R * batch.k}; {el:.1f} s, float64 numpy)"}
 
     if rank != 0:
