@@ -149,7 +149,9 @@ int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t
  *               MLA_FAULT_* bits for conditions it detects instead of trapping.
  * Numerics: FP8 QK^T and PV on the tensor cores with FP32 accumulation; FP32
  * online softmax in base 2 whose running max is kept while a new score
- * exceeds it by at most 8 (2^8, balanced-MLA page, module overview); P is fed
+ * exceeds it by at most 8 (2^8, balanced-MLA page, module overview) and, when
+ * it moves, is set 2 below the new maximum (P's small values then stay in
+ * E4M3's normal range); P is fed
  * to the PV product as FP8 E4M3, unscaled, as the sum of two E4M3 terms
  * (hi = e4m3(p), lo = e4m3(p - hi)); the normaliser is the FP32 sum of p. */
 int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,

@@ -25,6 +25,13 @@ constexpr int kOCols = 64;                        // TMEM columns per 128-dim ba
 constexpr int kSCol0 = 4 * kOCols;                // S^T buffers start after O^T
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
+// When a row's lazy max moves (a score beyond the old max + 8, base 2), it is
+// set kMaxLead below the tile's max instead of at it: P = 2^(x - max) then
+// reaches 2^kMaxLead on that tile and at most 2^8 (< 448) later, and more of
+// P's small values sit in E4M3's normal range (down to 2^-6) instead of its
+// subnormals, whose absolute step of 2^-9 dominated the output error. A larger
+// lead buys little more accuracy and moves the max (rescaling O) more often.
+constexpr float kMaxLead = 2.f;
 
 struct Ctl {
   uint64_t kv_full[kStages];   // TMA -> MMA: tile landed

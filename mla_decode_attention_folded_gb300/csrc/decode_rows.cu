@@ -3,7 +3,8 @@
 //
 // Same computation as decode_tc.cu (drafter-attention page, module overview
 // and `folded_decode`; balanced-MLA page, module overview): each work item's
-// split of the keys, softmax in base 2 with the +8 lazy max, P as two E4M3
+// split of the keys, softmax in base 2 with the +8 lazy max (moved to 2 below the
+// tile's max), P as two E4M3
 // terms, FP32 normaliser, BF16 out + log2 LSE or FP32 partial + LSE.
 //
 // Layout (ours): a job is (work item, 128-row block, half of the 512 output
@@ -218,8 +219,9 @@ __device__ void rows_softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* c
       const float tmax = smax * a.bmm1_log2;
       float alpha = 1.f;
       if (tmax > m + 8.f) {                        // the row's max moved by more than 8
-        alpha = m == -INFINITY ? 0.f : ex2(m - tmax);
-        m = tmax;
+        const float mn = tmax - kMaxLead;
+        alpha = m == -INFINITY ? 0.f : ex2(m - mn);
+        m = mn;
         l *= alpha;
       }
       // O holds tiles < gg: rows whose max moved scale their dims (whole warps

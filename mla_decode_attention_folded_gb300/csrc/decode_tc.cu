@@ -21,10 +21,11 @@
 //   each for the softmax and one value dim per 128-dim band for the epilogue.
 // * Softmax in base 2 with a lazily updated row max: the max moves only when a
 //   new score exceeds it by more than 8 (P <= 2^8, balanced-MLA page, module
-//   overview). P enters the PV MMA as FP8 E4M3, unscaled, split into two E4M3
-//   terms hi = e4m3(p), lo = e4m3(p - hi) (both FP8 operands: one E4M3 term
-//   alone misses the +-(2e-2 + 2e-2|ref|) bound on short requests). The
-//   normaliser is the FP32 sum of p.
+//   overview), and then to 2 below the tile's max (kMaxLead). P enters the PV
+//   MMA as FP8 E4M3, unscaled, split into two E4M3 terms hi = e4m3(p),
+//   lo = e4m3(p - hi) (both FP8 operands: one E4M3 term alone misses the
+//   +-(2e-2 + 2e-2|ref|) bound on short requests). The normaliser is the FP32
+//   sum of p.
 // * Every mbarrier wait is bounded (2 s); on expiry the CTA sets
 //   MLA_FAULT_WAIT_TIMEOUT in the status word, stops, drains its own copies and
 //   MMAs, frees TMEM and returns. No trap, no unbounded spin.
@@ -282,7 +283,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
         exceed |= xv[i] > ctl->m_run[i] + 8.f;
       }
       if (group_any(exceed)) {
-        // Rows whose max grew by more than 8: take the tile max as the new max.
+        // Rows whose max grew by more than 8: the new max is kMaxLead below the tile's.
 #pragma unroll
         for (int h = 0; h < NR / 32; ++h) {      // 32 rows at a time: fewer live registers
           float v[32];
@@ -296,7 +297,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
           const float tm = fmaxf(fmaxf(ctl->red[0][gt], ctl->red[1][gt]),
                                  fmaxf(ctl->red[2][gt], ctl->red[3][gt]));
           const float mo = ctl->m_run[gt];
-          const float mn = tm > mo + 8.f ? tm : mo;
+          const float mn = tm > mo + 8.f ? tm - kMaxLead : mo;
           ctl->vec[gt] = mo == -INFINITY ? 0.f : ex2(mo - mn);
           ctl->m_run[gt] = mn;
         }

@@ -153,6 +153,51 @@ def test_row_groups_match_oracle(lens, k, H):
             assert_close(out, lse, ref_o, ref_l, f"groups={groups} policy={policy}")
 
 
+@pytest.mark.parametrize("policy", [pl.BALANCED, pl.UNIFORM])
+def test_page_and_tile_boundaries(policy):
+    """Lengths on every page / tile boundary and the degenerate ones: empty, one
+    key, one key short of and past a page (64) and a tile (128)."""
+    lens = (0, 1, 63, 64, 65, 127, 128, 129, 191, 192, 255, 256, 257)
+    b = make_batch_from_lengths(lens, 3, 4, seed=17, scaling="amax", fill=-5)
+    ref_o, ref_l = oracle_full(b)
+    for mst in (64, 256):
+        out, lse, status, _ = run_decode(b, policy=policy, min_split_tokens=mst)
+        assert status == 0
+        assert_close(out, lse, ref_o, ref_l, f"boundaries mst={mst}")
+
+
+def test_one_row_per_request():
+    """k = 1, H = 1: a single query row per request (31 padding rows of the
+    32-row block)."""
+    b = make_batch_from_lengths((900, 3, 2000, 64), 1, 1, seed=19, scaling="amax")
+    ref_o, ref_l = oracle_full(b)
+    out, lse, status, _ = run_decode(b, min_split_tokens=64)
+    assert status == 0
+    assert_close(out, lse, ref_o, ref_l, "M=1")
+
+
+def test_maximum_row_groups():
+    """R * groups = 1024 row groups, the most the planner takes."""
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 400, size=512)
+    b = make_batch_from_lengths(lens, 2, 4, seed=23, scaling="amax")
+    ref_o, ref_l = oracle_full(b)
+    for groups in (1, 2):
+        out, lse, status, _ = run_decode(b, groups=groups, min_split_tokens=64)
+        assert status == 0
+        assert_close(out, lse, ref_o, ref_l, f"1024 row groups, groups={groups}")
+
+
+def test_maximum_rows_per_request():
+    """M = k * H = 4096 query rows per request (the largest M): the rows-as-M
+    kernel with 32 row blocks of 128 rows."""
+    b = make_batch_from_lengths((700, 130), 16, 256, seed=29, scaling="amax")
+    ref_o, ref_l = oracle_full(b)
+    out, lse, status, _ = run_decode(b, min_split_tokens=64)
+    assert status == 0
+    assert_close(out, lse, ref_o, ref_l, "M=4096")
+
+
 def test_folded_equals_unfolded():
     b = make_batch_from_lengths((900, 77, 2000), 4, 8, seed=5, scaling="amax")
     ref_o, ref_l = oracle_full(b)
