@@ -395,8 +395,11 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     group_sync();
     if (!(ok = wait_bar(&ctl->o_full, x & 1, ctl, a.status))) break;
     tc::fence_after_sync();
-    // Each 128-dim band of O^T goes through the P buffers (idle now: the last
-    // PV has finished) so that global stores are 16-byte row vectors.
+    // Each thread holds one output dim of a 128-dim band for every row (TMEM
+    // lane = dim), so for each row the warp's 32 lanes store 32 consecutive
+    // values. With 32 rows they go straight from registers to global memory;
+    // with 64 rows (register-bound) each band is staged through the P buffers
+    // (idle now: the last PV has finished) into 16-byte row vectors.
     uint8_t* stage = smem + C::kOffP;
     float sc[NR];                                  // per-row output scale
 #pragma unroll
@@ -420,26 +423,40 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
           }
         }
       }
-      if (jb.direct) {
-        uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
+      if constexpr (NR == 32) {
+        if (jb.direct) {
+          uint16_t* dst = a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128 + tl;
 #pragma unroll
-        for (int i = 0; i < NR; ++i)
-          st16[i * 128 + tl] = f32_to_bf16_bits(o[i] * sc[i]);
+          for (int i = 0; i < NR; ++i)
+            if (i < rows) dst[(long long)i * kDv] = f32_to_bf16_bits(o[i] * sc[i]);
+        } else {
+          float* dst = a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128 + tl;
+#pragma unroll
+          for (int i = 0; i < NR; ++i)
+            if (i < rows) dst[(long long)i * kDv] = o[i] * sc[i];
+        }
       } else {
-        float* st32 = reinterpret_cast<float*>(stage);
+        if (jb.direct) {
+          uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
 #pragma unroll
-        for (int i = 0; i < NR; ++i) st32[i * 128 + tl] = o[i] * sc[i];
+          for (int i = 0; i < NR; ++i) st16[i * 128 + tl] = f32_to_bf16_bits(o[i] * sc[i]);
+        } else {
+          float* st32 = reinterpret_cast<float*>(stage);
+#pragma unroll
+          for (int i = 0; i < NR; ++i) st32[i * 128 + tl] = o[i] * sc[i];
+        }
+        group_sync();
+        if (jb.direct)
+          copy_band<NR, true>(stage, reinterpret_cast<uint8_t*>(
+                                         a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128),
+                              rows, gt);
+        else
+          copy_band<NR, false>(stage,
+                               reinterpret_cast<uint8_t*>(
+                                   a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128),
+                               rows, gt);
+        group_sync();
       }
-      group_sync();
-      if (jb.direct)
-        copy_band<NR, true>(stage, reinterpret_cast<uint8_t*>(
-                                       a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128),
-                            rows, gt);
-      else
-        copy_band<NR, false>(stage, reinterpret_cast<uint8_t*>(
-                                        a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128),
-                             rows, gt);
-      group_sync();
     }
     tc::fence_before_sync();
     tc::mbar_arrive(&ctl->o_empty);
@@ -498,6 +515,16 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
   tc::fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
 
+  // While the plan runs, warm L2 with the block table (a prefetch returns no
+  // data, so whatever an earlier kernel writes there is still what is read).
+  // The short, latency-bound jobs of the 32-row kernel gain from it; the
+  // 64-row kernel is at its register limit.
+  if constexpr (NR == 32) {
+    const long long lines = ((long long)(a.R / a.groups) * a.max_pages * 4 + 127) / 128;
+    for (long long l = (long long)blockIdx.x * blockDim.x + threadIdx.x; l < lines;
+         l += (long long)gridDim.x * blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + l * 32));
+  }
   grid_dep_wait();      // the plan is complete; earlier readers of out/workspace are done
   grid_dep_launch();    // the reducer may launch; it still waits for this grid to finish
   if (warp == 0) {
