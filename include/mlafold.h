@@ -167,7 +167,10 @@ int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
  * (drafter-attention page, `DraftDcp`: exp2(lse - max) / sum in FP32, one
  * BF16 rounding). Arguments as for mla_folded_decode, same plan and workspace
  * (lse may be NULL: no LSE written).
- * Rows whose splits are all empty get out = 0 and lse = -inf. */
+ * Rows whose splits are all empty get out = 0 and lse = -inf.
+ * Ordering: launch it after that mla_folded_decode on the same stream (the
+ * decode between the two is what makes the plan complete when this kernel
+ * starts reading counts and work; it reads them while the decode finishes). */
 int32_t mla_split_combine(const mla_shape *shape, const int32_t *counts, const int32_t *work,
                           int32_t list_len, const void *workspace, size_t workspace_bytes,
                           float bmm2_scale, void *out, float *lse, mla_stream_t stream);

@@ -30,10 +30,12 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
   __shared__ int s_start[kMaxStarts];
   __shared__ int s_warp[kWarps];
   __shared__ int s_nreq;
-  grid_dep_wait();
-  grid_dep_launch();
   // Ordered compaction of the multi-split requests' first items: every CTA
   // must see the same list, in work-list order, to agree on row ownership.
+  // It runs before the wait for the decode, on SMs the decode has left: the
+  // work list and counts are the plan's, and every decode CTA passed its own
+  // wait for the plan's completion before this grid could launch (L2 reads,
+  // so no stale L1 line of an earlier step is seen).
   const int lane = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_nreq = 0;
   __syncthreads();
@@ -43,10 +45,10 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
     bool first = false;
     int r = 0;
     if (e < scan) {
-      const int w = work[e];
+      const int w = __ldcg(work + e);
       if (w >= 0 && (w & ((1 << kSplitBits) - 1)) == 0) {
         r = w >> kSplitBits;
-        first = r < R && counts[r] >= 2;
+        first = r < R && __ldcg(counts + r) >= 2;
       }
     }
     const unsigned ballot = __ballot_sync(0xffffffffu, first);
@@ -65,6 +67,8 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
     __syncthreads();
   }
   const int nreq = min(s_nreq, kMaxStarts);
+  grid_dep_wait();      // the decode's partials are complete
+  grid_dep_launch();
   constexpr int kDims = kDv / BANDS;          // dims per warp
   constexpr int kVec = kDims / 32 / 4;        // float4 per lane
   const long long total = (long long)nreq * M * BANDS;

@@ -233,25 +233,38 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
   tc::fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
 
-  grid_dep_wait();      // the decode's partials and one-split rows are complete
-  grid_dep_launch();
-
+  // Before the wait for the decode, on SMs the decode has left: the first
+  // head's W_UV (an input no kernel of the chain writes) and the scan of the
+  // plan's work list (every decode CTA passed its own wait for the plan's
+  // completion before this grid could launch; L2 reads, no stale L1 line).
+  int cur_h = -1, loads = 0;   // the W_UV head in shared memory, loads issued
+  if (warp == 0 && lane == 0 && t_begin < t_end) {
+    cur_h = t_begin / nblk;
+    for (int c = 0; c < kChunks; ++c) {
+      tc::mbar_arrive_expect_tx(&ctl->w_full[c], kWChunk);
+      tc::tma_load_2d(smem + kOffW + c * kWChunk, &tm_w, &ctl->w_full[c], c * 128,
+                      cur_h * kOut);
+    }
+    loads = 1;
+  }
   // First slot of every multi-split row group: split 0 followed by split 1 of
   // the same group at the head of the work list (multi-split items come first).
   const int scan = min(a.list_len, a.slots);
   for (int e = threadIdx.x; e + 1 < scan; e += blockDim.x) {
-    const int w = a.work[e];
-    if (w >= 0 && (w & ((1 << kSplitBits) - 1)) == 0 && a.work[e + 1] == w + 1) {
+    const int w = __ldcg(a.work + e);
+    if (w >= 0 && (w & ((1 << kSplitBits) - 1)) == 0 && __ldcg(a.work + e + 1) == w + 1) {
       const int r = w >> kSplitBits;
       if (r < a.plan_rows) s_start[r] = e;
     }
   }
   __syncthreads();
 
+  grid_dep_wait();      // the decode's partials and one-split rows are complete
+  grid_dep_launch();
+
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      int cur_h = -1, loads = 0;
       bool w_ready = false;
       int it = 0;
       for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
