@@ -38,7 +38,8 @@ constexpr int kXBytes = kChunks * kXChunk;     // one X buffer
 constexpr int kOffW = 0;                       // W_UV[h], eight chunks
 constexpr int kOffX = kChunks * kWChunk;       // two X buffers
 constexpr int kOffStart = kOffX + 2 * kXBytes; // first slot of each multi-split row group
-constexpr int kOffBar = kOffStart + kMaxR * 4;
+constexpr int kOffCount = kOffStart + kMaxR * 4;   // split count of every row group
+constexpr int kOffBar = kOffCount + kMaxR * 4;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;        // + control block, + alignment slack
 constexpr uint32_t kTmemCols = 2 * kTok;       // two FP32 accumulators of 32 columns
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kOut, kTok);
@@ -99,7 +100,8 @@ __device__ __forceinline__ int x_piece(int row, int i) {
 // `ready()` is called once, after the row's global loads and before its first
 // shared-memory write (it waits for the X buffer to be free); false = give up.
 template <typename Ready>
-__device__ __forceinline__ bool merged_row(const UvArgs& a, const int* s_start, int tau, int h,
+__device__ __forceinline__ bool merged_row(const UvArgs& a, const int* s_start,
+                                           const int* s_count, int tau, int h,
                                            int c, uint8_t* x, int row, Ready ready) {
   const uint4 zero = make_uint4(0, 0, 0, 0);
   int n = 0, r = 0, t = 0, i = 0, mg = 0;
@@ -109,7 +111,7 @@ __device__ __forceinline__ bool merged_row(const UvArgs& a, const int* s_start, 
     const int kg = a.k / a.groups;
     i = r * a.groups + t / kg;                  // the row group that decoded this token
     mg = (t % kg) * a.H + h;                    // its row within that group
-    n = a.counts[i];
+    n = s_count[i];
   }
   if (tau >= a.T) {                             // rows past the batch stay zero
     if (!ready()) return false;
@@ -203,6 +205,7 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
                                              ~uintptr_t(1023));
   UvCtl* ctl = reinterpret_cast<UvCtl*>(smem + kOffBar);
   int* s_start = reinterpret_cast<int*>(smem + kOffStart);
+  int* s_count = reinterpret_cast<int*>(smem + kOffCount);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // This CTA's tiles: a contiguous, head-major range of (head, token block).
   const int nblk = (int)cdiv(a.T, kTok);
@@ -247,6 +250,7 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
     }
     loads = 1;
   }
+  for (int i = threadIdx.x; i < a.plan_rows; i += blockDim.x) s_count[i] = __ldcg(a.counts + i);
   // First slot of every multi-split row group: split 0 followed by split 1 of
   // the same group at the head of the work list (multi-split items come first).
   const int scan = min(a.list_len, a.slots);
@@ -350,7 +354,7 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
         return it_now < 2 ||
                uv_wait(&ctl->x_empty[it_now & 1], ((it_now - 2) >> 1) & 1, ctl, a.status);
       };
-      if (!(ok = merged_row(a, s_start, tok0 + row, h, c, smem + kOffX + buf * kXBytes, row,
+      if (!(ok = merged_row(a, s_start, s_count, tok0 + row, h, c, smem + kOffX + buf * kXBytes, row,
                             x_free)))
         break;
       tc::fence_proxy_async_smem();
