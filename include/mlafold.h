@@ -102,8 +102,9 @@ typedef struct {
 } mla_shape;
 
 /* Capacity, in entries, of the work list `work` that mla_plan_splits fills
- * for this shape: enough for any length vector. Returns the capacity (>= 1)
- * or a negative mla_status. Host only; launches nothing. */
+ * for this shape: enough items for any length vector, plus two trailing
+ * entries the decode uses as job counters (see mla_folded_decode). Returns
+ * the capacity (>= 3) or a negative mla_status. Host only; launches nothing. */
 int32_t mla_plan_list_len(const mla_shape *shape);
 
 /* Bytes of split-KV workspace mla_folded_decode and mla_split_combine need for
@@ -127,7 +128,12 @@ int32_t mla_workspace_bytes(const mla_shape *shape, size_t *bytes);
 int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t *counts,
                         int32_t *work, int32_t list_len, mla_stream_t stream);
 
-/* Split-KV decode of the planned work list.
+/* Split-KV decode of the planned work list. Persistent CTAs take one job
+ * each (a work item's block of query rows), then claim further jobs in list
+ * order from a counter kept in the two entries after the items in `work`
+ * (the plan leaves them at -1; the decode counts them down and its last CTA
+ * puts them back to -1), so one plan serves any number of decodes in stream
+ * order. Decodes that share one `work` array must not run concurrently.
  *   q           [R*k, H, 576] FP8 E4M3, device, 16-byte aligned: the queries in the
  *               stock token-major layout (= the folded [R, M, 576] view).
  *   kv          [num_pages, 64, 576] FP8 E4M3, device, 16-byte aligned: the
@@ -157,7 +163,7 @@ int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t
 int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
                           const int32_t *block_table, const int32_t *seq_lens,
                           float bmm1_scale, float bmm2_scale, const int32_t *counts,
-                          const int32_t *work, int32_t list_len, void *workspace,
+                          int32_t *work, int32_t list_len, void *workspace,
                           size_t workspace_bytes, void *out, float *lse, int32_t *status,
                           mla_stream_t stream);
 
@@ -237,7 +243,7 @@ int32_t mla_lse_merge(int32_t S, int32_t rows, const void *parts_out, const floa
 int32_t mla_folded_decode_noalloc(const mla_shape *shape, const void *q, const void *kv,
                                   const int32_t *block_table, const int32_t *seq_lens,
                                   float bmm1_scale, float bmm2_scale, const int32_t *counts,
-                                  const int32_t *work, int32_t list_len, void *out, float *lse,
+                                  int32_t *work, int32_t list_len, void *out, float *lse,
                                   int32_t *status, mla_stream_t stream);
 
 /* Bits the decode kernel ORs into *status. */

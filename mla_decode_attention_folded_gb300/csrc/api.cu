@@ -72,7 +72,7 @@ int32_t mla_plan_splits(const mla_shape* shape, const int32_t* seq_lens, int32_t
 
 int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
                           const int32_t* block_table, const int32_t* seq_lens, float bmm1_scale,
-                          float bmm2_scale, const int32_t* counts, const int32_t* work,
+                          float bmm2_scale, const int32_t* counts, int32_t* work,
                           int32_t list_len, void* workspace, size_t workspace_bytes_given,
                           void* out, float* lse, int32_t* status, mla_stream_t stream) {
   int st = check_shape(shape);
@@ -99,6 +99,7 @@ int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
   a.seq_lens = seq_lens;
   a.counts = counts;
   a.work = work;
+  a.sched = work + plan_items(*shape);
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                     partial_out_bytes(slots, M))
@@ -113,7 +114,7 @@ int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
   a.groups = shape_groups(*shape);
   a.max_pages = shape->max_pages;
   a.num_pages = shape->num_pages;
-  a.list_len = list_len;
+  a.items = plan_items(*shape);
   a.slots = slots;
   cudaError_t e = launch_decode(*shape, a, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

@@ -33,6 +33,12 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;
 // lead buys little more accuracy and moves the max (rescaling O) more often.
 constexpr float kMaxLead = 2.f;
 
+// Per-job facts, from the plan (read_job). item < 0: no more jobs.
+struct Job {
+  int r, blk, item, j0, j1, ntiles;
+  bool direct, skip;
+};
+
 struct Ctl {
   uint64_t kv_full[kStages];   // TMA -> MMA: tile landed
   uint64_t pv_done[kStages];   // MMA -> TMA, softmax: PV of a tile finished (stage, P free)
@@ -42,6 +48,9 @@ struct Ctl {
   uint64_t q_full, q_empty;    // Q block of the job
   uint64_t o_full, o_empty;    // O^T of the job
   uint64_t drain;
+  uint64_t job_full[2];        // producer -> other roles: the next job is in job[]
+  uint64_t job_empty[2];       // other roles -> producer: job read
+  Job job[2];
   uint32_t tmem_base;
   int abort_flag;
   float m_run[64];             // running row max (base-2 scores)
@@ -79,11 +88,6 @@ __device__ __forceinline__ bool group_any(bool pred) {
   return r != 0;
 }
 
-// Per-job facts every role derives identically from the plan.
-struct Job {
-  int r, blk, item, j0, j1, ntiles;
-  bool direct, skip;
-};
 
 __device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, bool report) {
   Job jb;
@@ -116,6 +120,64 @@ __device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, 
   return jb;
 }
 
+// ---------------------------------------------------------------- job claiming
+// A CTA's first job is its index; after that its producer claims jobs in
+// work-list order from a counter (the entry after the items), so a CTA that
+// finishes early takes more of the list, which runs longest request first.
+// The counter counts down from -1: claim k (from 0) is job gridDim.x + k.
+__device__ __forceinline__ int claim_job(const DecodeArgs& a, int lane) {
+  int k = 0;
+  if (lane == 0) k = -1 - atomicAdd(a.sched, -1);
+  return (int)gridDim.x + __shfl_sync(0xffffffffu, k, 0);
+}
+
+// The producer hands each job, or one with item -1 at the end, to the MMA and
+// softmax roles through a two-slot ring (lane 0 of the producer).
+__device__ __forceinline__ bool publish_job(Ctl* ctl, uint32_t seq, const Job& jb,
+                                            int32_t* status) {
+  const int b = seq & 1;
+  if (seq >= 2 && !wait_bar(&ctl->job_empty[b], ((seq >> 1) - 1) & 1, ctl, status)) return false;
+  volatile Job* slot = &ctl->job[b];
+  slot->r = jb.r;
+  slot->blk = jb.blk;
+  slot->item = jb.item;
+  slot->j0 = jb.j0;
+  slot->j1 = jb.j1;
+  slot->ntiles = jb.ntiles;
+  slot->direct = jb.direct;
+  slot->skip = jb.skip;
+  tc::mbar_arrive(&ctl->job_full[b]);       // release: the job is visible to the waiters
+  return true;
+}
+__device__ __forceinline__ bool take_job(Ctl* ctl, uint32_t seq, int32_t* status, Job& jb) {
+  const int b = seq & 1;
+  if (!wait_bar(&ctl->job_full[b], (seq >> 1) & 1, ctl, status)) return false;
+  const volatile Job* slot = &ctl->job[b];
+  jb.r = slot->r;
+  jb.blk = slot->blk;
+  jb.item = slot->item;
+  jb.j0 = slot->j0;
+  jb.j1 = slot->j1;
+  jb.ntiles = slot->ntiles;
+  jb.direct = slot->direct;
+  jb.skip = slot->skip;
+  tc::mbar_arrive(&ctl->job_empty[b]);
+  return true;
+}
+
+// Lane 0 of the producer, after the CTA's last claim: count the CTA out; the
+// last one resets both counters to -1 for the next decode of the same plan.
+// The other roles are still finishing their last tiles meanwhile.
+__device__ __forceinline__ void finish_jobs(const DecodeArgs& a) {
+  __threadfence();
+  const int done = -1 - atomicAdd(a.sched + 1, -1);
+  if (done == (int)gridDim.x - 1) {
+    __threadfence();
+    atomicExch(a.sched, -1);
+    atomicExch(a.sched + 1, -1);
+  }
+}
+
 // ---------------------------------------------------------------- producer
 // Runs on all 32 lanes of warp 0: the lanes fetch the job's block-table
 // entries 32 at a time (lane i holds page i of the chunk, checked against the
@@ -134,7 +196,7 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
   uint32_t g = 0, x = 0;
   int last_q_parity = -1;
   int last_kv_parity[kStages] = {-1, -1};
-  const int njobs = a.list_len * nb;
+  const int njobs = a.items * nb;
   bool ok = true;
   auto wait0 = [&](uint64_t* bar, uint32_t parity) {
     int r = 1;
@@ -154,11 +216,30 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
     }
     return p;
   };
-  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
-    const int item = job / nb, blk = job % nb;
-    if (a.work[item] < 0) break;
-    const Job jb = read_job(a, item, blk, lane == 0);
-    if (jb.skip || jb.ntiles == 0) continue;
+  int job = (int)blockIdx.x;
+  for (uint32_t seq = 0; ok; ++seq) {
+    Job jb;
+    int blk = 0;
+    bool have = false;
+    while (job < njobs) {                        // the next job that is not malformed
+      const int item = job / nb;
+      blk = job % nb;
+      if (a.work[item] < 0) break;               // past the last item (the list is compact)
+      jb = read_job(a, item, blk, lane == 0);
+      if (!jb.skip) {
+        have = true;
+        break;
+      }
+      job = claim_job(a, lane);
+    }
+    if (!have) jb.item = -1;
+    int pub = 1;
+    if (lane == 0) pub = publish_job(ctl, seq, jb, a.status) ? 1 : 0;
+    if (!(ok = __shfl_sync(0xffffffffu, pub, 0) != 0) || !have) break;
+    if (jb.ntiles == 0) {                        // an empty split: the softmax role writes it
+      job = claim_job(a, lane);
+      continue;
+    }
     int cur = fetch(jb, 0), nxt = fetch(jb, 1);
     if (x > 0 && !(ok = wait0(&ctl->q_empty, (x - 1) & 1))) break;
     if (lane == 0) {
@@ -216,8 +297,11 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
         }
       }
     }
+    if (!ok) break;
     ++x;
+    job = claim_job(a, lane);
   }
+  if (lane == 0) finish_jobs(a);
   // Never leave with copies in flight into this CTA's shared memory.
   if (!ok && lane == 0) {
     const unsigned long long t0 = tc::globaltimer_ns();

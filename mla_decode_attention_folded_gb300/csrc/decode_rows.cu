@@ -53,7 +53,6 @@ __device__ void rows_mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, ui
                                 int nb) {
   const uint32_t s_kv = tc::smem_u32(smem), s_q = tc::smem_u32(smem + kOffQ);
   uint32_t g = 0, x = 0;
-  const int njobs = a.list_len * nb;
   bool ok = true;
 
   auto issue_s = [&](uint32_t gg) {
@@ -88,10 +87,10 @@ __device__ void rows_mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, ui
     tc::mma_commit(&ctl->pv_done[st]);
   };
 
-  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
-    const int item = job / nb, sub = job % nb;
-    if (a.work[item] < 0) break;
-    const Job jb = read_job(a, item, sub, false);
+  for (uint32_t seq = 0; ok; ++seq) {
+    Job jb;
+    if (!(ok = take_job(ctl, seq, a.status, jb)) || jb.item < 0) break;
+    const int sub = jb.blk;
     if (jb.skip || jb.ntiles == 0) continue;
     const int half = sub & 1;
     if (!(ok = wait_bar(&ctl->q_full, x & 1, ctl, a.status))) break;
@@ -160,13 +159,12 @@ __device__ void rows_softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* c
   const int tl = quarter * 32 + lane;             // this thread's query row (and key row)
   const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
   uint32_t g = 0, x = 0;
-  const int njobs = a.list_len * nb;
   bool ok = true;
 
-  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
-    const int item = job / nb, sub = job % nb;
-    if (a.work[item] < 0) break;
-    const Job jb = read_job(a, item, sub, false);
+  for (uint32_t seq = 0; ok; ++seq) {
+    Job jb;
+    if (!(ok = take_job(ctl, seq, a.status, jb)) || jb.item < 0) break;
+    const int sub = jb.blk;
     if (jb.skip) continue;
     const int half = sub & 1;
     const int m0 = (sub >> 1) * kQRows;
@@ -353,6 +351,10 @@ decode_rows_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv
     tc::mbar_init(&ctl->o_full, 1);
     tc::mbar_init(&ctl->o_empty, kGroup);
     tc::mbar_init(&ctl->drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl->job_full[b], 1);
+      tc::mbar_init(&ctl->job_empty[b], 1 + kGroup);   // the MMA thread + the softmax group
+    }
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -406,7 +408,7 @@ cudaError_t launch_decode_rows(const mla_shape& s, const DecodeArgs& a, cudaStre
   cudaError_t e = set_smem(decode_rows_kernel, smem_bytes, attr_set);
   if (e != cudaSuccess) return e;
   const int nb = row_blocks(a.M);
-  const long long jobs = (long long)a.list_len * nb;
+  const long long jobs = (long long)a.items * nb;
   const int grid = (int)(jobs < s.num_ctas ? jobs : s.num_ctas);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid > 0 ? grid : 1);

@@ -8,7 +8,10 @@
 // BF16 out + base-2 LSE (one split) or as an FP32 partial + LSE (several).
 //
 // Design (ours; the pages' kernels are prior art only):
-// * Persistent CTAs, one per SM, walk the (item, row block) jobs round-robin.
+// * Persistent CTAs, one per SM: CTA b takes (item, row block) job b, then
+//   claims further jobs in list order from a counter (longest requests
+//   first), so CTAs that finish early take more of the list; warp 0 claims
+//   and hands each job to the other roles through a two-slot ring.
 // * Swap-AB: keys are the MMA's M dimension (128 per tile = two pages) and
 //   query rows its N, so M = k*H of 32..448 needs no padding to 128 and the
 //   whole O^T accumulator (512 dims x N rows) plus two S^T buffers fit TMEM.
@@ -80,7 +83,6 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
   const uint32_t s_kv = tc::smem_u32(smem), s_q = tc::smem_u32(smem + C::kOffQ);
   const uint32_t s_p = tc::smem_u32(smem + C::kOffP);
   uint32_t g = 0, x = 0;
-  const int njobs = a.list_len * nb;
   bool ok = true;
 
   auto issue_s = [&](uint32_t gg) {
@@ -132,10 +134,10 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
     tc::mma_commit(&ctl->pv_done[st]);
   };
 
-  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
-    const int item = job / nb, blk = job % nb;
-    if (a.work[item] < 0) break;
-    const Job jb = read_job(a, item, blk, false);
+  for (uint32_t seq = 0; ok; ++seq) {
+    Job jb;
+    if (!(ok = take_job(ctl, seq, a.status, jb)) || jb.item < 0) break;
+    const int blk = jb.blk;
     if (jb.skip || jb.ntiles == 0) continue;
     if (!(ok = wait_bar(&ctl->q_full, x & 1, ctl, a.status))) break;
     // Issue S(t) as soon as its tile landed and its S buffer is free, and PV(t)
@@ -226,14 +228,13 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
   const int gt = threadIdx.x - 64;                // 0..127 within the group
   const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
   uint32_t g = 0, x = 0;
-  const int njobs = a.list_len * nb;
   bool ok = true;
   float lp[NR];                                   // this key's share of each row sum
 
-  for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
-    const int item = job / nb, blk = job % nb;
-    if (a.work[item] < 0) break;
-    const Job jb = read_job(a, item, blk, false);
+  for (uint32_t seq = 0; ok; ++seq) {
+    Job jb;
+    if (!(ok = take_job(ctl, seq, a.status, jb)) || jb.item < 0) break;
+    const int blk = jb.blk;
     if (jb.skip) continue;
     const int m0 = blk * NR;
     const int rows = min(NR, a.M - m0);
@@ -497,6 +498,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
     tc::mbar_init(&ctl->o_full, 1);
     tc::mbar_init(&ctl->o_empty, 128);
     tc::mbar_init(&ctl->drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl->job_full[b], 1);
+      tc::mbar_init(&ctl->job_empty[b], 1 + 128);   // the MMA thread + the softmax group
+    }
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -561,7 +566,7 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
   cudaError_t e = set_smem(decode_tc_kernel<NR>, smem_bytes, attr_set);
   if (e != cudaSuccess) return e;
   const int nb = row_blocks(a.M);
-  const long long jobs = (long long)a.list_len * nb;
+  const long long jobs = (long long)a.items * nb;
   const int grid = (int)(jobs < s.num_ctas ? jobs : s.num_ctas);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid > 0 ? grid : 1);

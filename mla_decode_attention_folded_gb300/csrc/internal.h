@@ -49,16 +49,22 @@ __host__ __device__ inline int uniform_splits(int R, int M, int num_ctas, int ma
 inline int shape_groups(const mla_shape& s) { return s.groups > 0 ? s.groups : 1; }
 inline int plan_rows(const mla_shape& s) { return s.R * shape_groups(s); }
 inline int group_rows(const mla_shape& s) { return (s.k / shape_groups(s)) * s.H; }
-inline int plan_list_len(const mla_shape& s) {
+// Work-list entries for items (the plan's bound on their number).
+inline int plan_items(const mla_shape& s) {
   const int R = plan_rows(s), M = group_rows(s);
   if (s.policy == MLA_POLICY_BALANCED) return plan_units(M, s.num_ctas) + R;
   return R * uniform_splits(R, M, s.num_ctas, s.max_splits);
 }
+// After the items, the decode's two job counters (claimed jobs, finished
+// CTAs): the plan sets them to -1 with the rest of the padding, they count
+// down during a decode, and its last CTA sets them back to -1.
+constexpr int kSchedWords = 2;
+inline int plan_list_len(const mla_shape& s) { return plan_items(s) + kSchedWords; }
 // Bound on items of multi-split requests; they occupy work-list slots [0, slots).
 inline int partial_slots(const mla_shape& s) {
   const int R = plan_rows(s), M = group_rows(s);
   if (s.policy == MLA_POLICY_BALANCED) {
-    int a = plan_list_len(s), b = 2 * plan_units(M, s.num_ctas);
+    int a = plan_items(s), b = 2 * plan_units(M, s.num_ctas);
     return a < b ? a : b;
   }
   int u = uniform_splits(R, M, s.num_ctas, s.max_splits);
@@ -89,6 +95,7 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   const int32_t* counts;
   const int32_t* work;
+  int32_t* sched;    // work + items: the job counters
   float* part_o;     // [slots][M][512]
   float* part_lse;   // [slots][M]
   uint16_t* out;     // [R][M][512] bf16 bits
@@ -96,7 +103,7 @@ struct DecodeArgs {
   int32_t* status;   // may be null
   float bmm1_log2;   // bmm1_scale * log2(e)
   float bmm2;
-  int R, M, max_pages, num_pages, list_len, slots;   // R, M: row groups, rows per group
+  int R, M, max_pages, num_pages, items, slots;   // R, M: row groups, rows per group
   int groups;          // row group g reads request g / groups
 };
 

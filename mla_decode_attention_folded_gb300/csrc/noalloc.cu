@@ -48,7 +48,7 @@ extern "C" int32_t mla_folded_decode_noalloc(const mla_shape* shape, const void*
                                              const void* kv, const int32_t* block_table,
                                              const int32_t* seq_lens, float bmm1_scale,
                                              float bmm2_scale, const int32_t* counts,
-                                             const int32_t* work, int32_t list_len, void* out,
+                                             int32_t* work, int32_t list_len, void* out,
                                              float* lse, int32_t* status, mla_stream_t stream) {
   size_t need = 0;
   int32_t st = mla_workspace_bytes(shape, &need);

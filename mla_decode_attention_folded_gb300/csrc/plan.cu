@@ -52,7 +52,7 @@ __device__ int block_max(int v, int* red) {
 __global__ void __launch_bounds__(kThreads, 1)
 plan_kernel(const int32_t* __restrict__ seq_lens, int R, int groups, int M, int num_ctas,
             int minp, int max_splits, int policy, int32_t* __restrict__ counts,
-            int32_t* __restrict__ work, int list_len) {
+            int32_t* __restrict__ work, int items, int list_len) {
   __shared__ int s_len[kThreads];
   __shared__ int s_n_by_rank[kThreads];
   __shared__ long long s_red64[32];
@@ -149,7 +149,7 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int R, int groups, int M, int 
   if (live) {
     const int start = s_n_by_rank[rank];
     for (int s = 0; s < n; ++s)
-      if (start + s < list_len) work[start + s] = (i << kSplitBits) | s;
+      if (start + s < items) work[start + s] = (i << kSplitBits) | s;
     counts[i] = n;
   }
   for (int e = total + i; e < list_len; e += blockDim.x) work[e] = -1;
@@ -171,7 +171,8 @@ cudaError_t launch_plan(const mla_shape& s, const int32_t* seq_lens, int32_t* co
   cfg.numAttrs = 1;
   const int minp = (int)cdiv(s.min_split_tokens, kPage) < 1 ? 1 : (int)cdiv(s.min_split_tokens, kPage);
   return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, R, shape_groups(s), group_rows(s),
-                            s.num_ctas, minp, s.max_splits, s.policy, counts, work, list_len);
+                            s.num_ctas, minp, s.max_splits, s.policy, counts, work,
+                            plan_items(s), list_len);
 }
 
 }  // namespace mlafold

@@ -41,7 +41,7 @@ def test_planner_bit_exact_on_workloads(name, policy):
     lens = draw_lengths(w.lengths, w.R, gen) if b is None else b.seq_lens.numpy()
     for G in (8, _sms()):
         c, wk = _gpu_plan(lens, w.M, G, 256, 64, policy)
-        c2, wk2 = pl.plan(lens, w.M, G, 256, 64, policy)
+        c2, wk2 = pl.plan(lens, w.M, G, 256, 64, policy, capacity=len(wk))
         assert np.array_equal(c, c2) and np.array_equal(wk, wk2)
 
 
@@ -65,7 +65,7 @@ def test_planner_bit_exact_random():
         ms = int(rng.choice([1, 2, 64, 4096]))
         policy = int(rng.integers(0, 2))
         c, wk = _gpu_plan(lens, M, G, mst, ms, policy)
-        c2, wk2 = pl.plan(lens, M, G, mst, ms, policy)
+        c2, wk2 = pl.plan(lens, M, G, mst, ms, policy, capacity=len(wk))
         assert np.array_equal(c, c2), (trial, R, M, G)
         assert np.array_equal(wk, wk2), (trial, R, M, G)
 
@@ -132,7 +132,8 @@ def test_planner_bit_exact_with_row_groups():
         counts = torch.zeros(R * groups, dtype=torch.int32, device="cuda")
         work = torch.full((n,), 7, dtype=torch.int32, device="cuda")
         mla.plan_splits(s, torch.tensor(lens.astype(np.int32), device="cuda"), counts, work)
-        c2, w2 = pl.plan(np.repeat(lens, groups), (k // groups) * H, G, 256, 64, policy)
+        c2, w2 = pl.plan(np.repeat(lens, groups), (k // groups) * H, G, 256, 64, policy,
+                         capacity=n)
         assert np.array_equal(counts.cpu().numpy(), c2), trial
         assert np.array_equal(work.cpu().numpy(), w2), trial
 
@@ -217,6 +218,39 @@ def test_many_splits_of_one_request():
     assert_close(out, lse, ref_o, ref_l, "many splits")
 
 
+@pytest.mark.parametrize("lens,k,H,G", [
+    ((6000,) + (300,) * 30 + (0, 90), 4, 8, 5),     # 32-row kernel, an empty request
+    ((4000, 2500) + (700,) * 12, 7, 8, 7),         # 64-row kernel
+    ((3000, 1500, 400, 64), 2, 64, 3),             # rows-as-M kernel (128 rows, two halves)
+])
+def test_claimed_jobs_and_repeated_decodes_of_one_plan(lens, k, H, G):
+    """Far more jobs than CTAs: after its first job a CTA claims the next ones
+    in list order from the counters after the items. Three decodes of one plan
+    agree bit for bit and with the oracle, and each leaves the work list as the
+    plan wrote it (both counters back at -1)."""
+    b = make_batch_from_lengths(lens, k, H, seed=sum(lens) + G, scaling="amax")
+    d = to_device(b)
+    eng = mla.FoldedMla(b.R, b.k, b.H, d["bt"].shape[1], d["kv"].shape[0], "cuda", num_ctas=G,
+                        min_split_tokens=64)
+    bmm1, bmm2 = bmm_scales(b)
+    eng.plan(d["lens"])
+    torch.cuda.synchronize()
+    planned = eng.work.cpu().clone()
+    assert torch.all(planned[-2:] == -1)
+    runs = []
+    for _ in range(3):
+        out, lse = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2)
+        torch.cuda.synchronize()
+        assert torch.equal(eng.work.cpu(), planned)
+        runs.append((out.clone(), lse.clone()))
+    assert int(eng.status.item()) == 0
+    for o, l in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
+    ref_o, ref_l = oracle_full(b)
+    assert_close(runs[0][0].float().cpu(), runs[0][1].cpu(), ref_o, ref_l,
+                 f"lens={len(lens)} requests k={k} H={H} G={G}")
+
+
 def test_out_of_range_page_sets_status_without_fault():
     b = make_batch_from_lengths((300, 100), 2, 8, seed=3, scaling="amax")
     b.block_table[0, 2] = b.kv.shape[0] + 1000          # inside request 0's pages
@@ -271,7 +305,8 @@ def test_combine_on_oracle_partials():
     b = make_batch_from_lengths((3000, 700, 64, 0), 2, 8, seed=77, scaling="amax")
     G = 16
     s = mla.make_shape(b.R, b.k, b.H, b.block_table.shape[1], b.kv.shape[0], G, 64, 64)
-    counts, work = pl.plan(b.seq_lens.numpy(), b.M, G, 64, 64, pl.BALANCED)
+    counts, work = pl.plan(b.seq_lens.numpy(), b.M, G, 64, 64, pl.BALANCED,
+                           capacity=mla.plan_list_len(s))
     slots = pl.partial_slots(b.R, b.M, G, pl.BALANCED, 64)
     ws = torch.zeros(mla.workspace_bytes(s), dtype=torch.uint8)
     po_bytes = (slots * b.M * 512 * 4 + 255) // 256 * 256

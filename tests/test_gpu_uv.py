@@ -83,7 +83,8 @@ def test_uv_on_oracle_partials():
     b = make_batch_from_lengths((3000, 700, 64, 0, 2500), 2, 8, seed=77, scaling="amax")
     G = 16
     s = mla.make_shape(b.R, b.k, b.H, b.block_table.shape[1], b.kv.shape[0], G, 64, 64)
-    counts, work = pl.plan(b.seq_lens.numpy(), b.M, G, 64, 64, pl.BALANCED)
+    counts, work = pl.plan(b.seq_lens.numpy(), b.M, G, 64, 64, pl.BALANCED,
+                           capacity=mla.plan_list_len(s))
     slots = pl.partial_slots(b.R, b.M, G, pl.BALANCED, 64)
     ws = torch.zeros(mla.workspace_bytes(s), dtype=torch.uint8)
     po_bytes = (slots * b.M * 512 * 4 + 255) // 256 * 256
