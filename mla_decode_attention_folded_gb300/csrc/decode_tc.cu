@@ -137,7 +137,6 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
   for (uint32_t seq = 0; ok; ++seq) {
     Job jb;
     if (!(ok = take_job(ctl, seq, a.status, jb)) || jb.item < 0) break;
-    const int blk = jb.blk;
     if (jb.skip || jb.ntiles == 0) continue;
     if (!(ok = wait_bar(&ctl->q_full, x & 1, ctl, a.status))) break;
     // Issue S(t) as soon as its tile landed and its S buffer is free, and PV(t)
