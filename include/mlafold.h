@@ -85,10 +85,10 @@ typedef struct {
   int32_t k;                /* query tokens per request (draft block), >= 1                */
   int32_t H;                /* heads per token, >= 1; M = k*H rows per request, <= 4096    */
   int32_t page_size;        /* tokens per cache page; must be 64                           */
-  int32_t max_pages;        /* entries per block_table row (row pitch), >= 1               */
+  int32_t max_pages;        /* entries per block_table row (row pitch), 1 .. 2^25 - 1      */
   int32_t num_pages;        /* pages in the cache, >= 1, < 2^25                            */
   int32_t num_ctas;         /* persistent CTAs the plan targets and the decode launches;
-                               normally the device's SM count, 1..65535                    */
+                               normally the device's SM count, 1..2048                     */
   int32_t min_split_tokens; /* smallest split a long request is cut into, >= 1 (e.g. 256)  */
   int32_t max_splits;       /* largest split count of one request, 1..4096 (e.g. 64)       */
   int32_t policy;           /* mla_policy                                                   */

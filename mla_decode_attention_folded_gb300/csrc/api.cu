@@ -20,7 +20,9 @@ int check_shape(const mla_shape* s) {
   if (s->k % groups != 0 || (long long)s->R * groups > kMaxR) return MLA_ERR_SHAPE;
   const long long M = (long long)s->k * s->H;
   if (M > kMaxM) return MLA_ERR_SHAPE;
-  if (s->max_pages < 1 || s->num_pages < 1 || s->num_pages >= (1 << 25)) return MLA_ERR_SHAPE;
+  if (s->max_pages < 1 || s->max_pages >= (1 << 25) || s->num_pages < 1 ||
+      s->num_pages >= (1 << 25))
+    return MLA_ERR_SHAPE;
   if (s->num_ctas < 1 || s->num_ctas > 2048) return MLA_ERR_SHAPE;
   if (s->min_split_tokens < 1) return MLA_ERR_SHAPE;
   if (s->max_splits < 1 || s->max_splits > (1 << kSplitBits)) return MLA_ERR_SHAPE;

@@ -17,6 +17,10 @@ HEADER = os.path.join(os.path.dirname(__file__), "..", "include", "mlafold.h")
 SCHED_WORDS = 2
 
 
+def library_len(items):
+    return items + SCHED_WORDS
+
+
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -39,7 +43,7 @@ def test_library_exports_every_declared_symbol():
 def test_sizes_match_oracle_planner(R, k, H, G, policy, ms):
     s = mla.make_shape(R, k, H, 10, 100, G, 256, ms, policy)
     M = k * H
-    assert mla.plan_list_len(s) == pl.list_len(R, M, G, policy, ms) + SCHED_WORDS
+    assert mla.plan_list_len(s) == library_len(pl.list_len(R, M, G, policy, ms))
     slots = pl.partial_slots(R, M, G, policy, ms)
     align = lambda x: (x + 255) // 256 * 256
     want = 0 if slots == 0 else align(slots * M * 512 * 4) + align(slots * M * 4)
@@ -49,7 +53,8 @@ def test_sizes_match_oracle_planner(R, k, H, G, policy, ms):
 @pytest.mark.parametrize("field,value,code", [
     ("page_size", 32, -5), ("R", 0, -2), ("R", 1025, -2), ("k", 0, -2), ("H", 0, -2),
     ("H", 5000, -2), ("num_ctas", 0, -2), ("max_splits", 4097, -2), ("policy", 7, -2),
-    ("min_split_tokens", 0, -2), ("num_pages", 0, -2), ("max_pages", 0, -2)])
+    ("min_split_tokens", 0, -2), ("num_pages", 0, -2), ("max_pages", 0, -2),
+    ("max_pages", 1 << 25, -2)])
 def test_bad_shape_rejected_on_host(field, value, code):
     s = mla.make_shape(4, 2, 8, 10, 100, 152)
     setattr(s, field, value)
@@ -95,7 +100,7 @@ def test_row_group_sizes_match_oracle(R, k, H, groups):
     for policy in (pl.BALANCED, pl.UNIFORM):
         s = mla.make_shape(R, k, H, 10, 100, 152, 256, 64, policy, groups)
         Rg, Mg = R * groups, (k // groups) * H
-        assert mla.plan_list_len(s) == pl.list_len(Rg, Mg, 152, policy, 64) + SCHED_WORDS
+        assert mla.plan_list_len(s) == library_len(pl.list_len(Rg, Mg, 152, policy, 64))
         slots = pl.partial_slots(Rg, Mg, 152, policy, 64)
         align = lambda x: (x + 255) // 256 * 256
         want = 0 if slots == 0 else align(slots * Mg * 512 * 4) + align(slots * Mg * 4)
