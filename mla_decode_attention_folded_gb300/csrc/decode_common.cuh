@@ -16,7 +16,6 @@ namespace dec {
 
 constexpr int kTileKeys = 128;                    // keys per MMA tile (two pages)
 constexpr int kStages = 2;                        // KV tiles in flight
-constexpr int kThreads = 192;                     // 6 warps
 constexpr int kChunkBytes = kTileKeys * 128;      // one 128-dim latent band of a tile
 constexpr int kRopeBytes = kTileKeys * 64;        // the 64 rope dims of a tile
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;     // 73728
@@ -74,19 +73,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ct
   }
 }
 
-__device__ __forceinline__ void group_sync() {   // the 128 softmax threads
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-__device__ __forceinline__ bool group_any(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, 2, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r)
-      : "r"((uint32_t)pred)
-      : "memory");
-  return r != 0;
-}
 
 
 __device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, bool report) {

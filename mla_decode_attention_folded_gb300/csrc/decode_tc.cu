@@ -20,8 +20,10 @@
 //                          the same shared-memory tile, read MN-major)
 // * Warp roles: warp 0 issues TMA (per-page gathers through the block table
 //   into a 2-stage ring of 128-key tiles; Q block once per job); warp 1 issues
-//   the MMAs and owns TMEM; warps 2-5 (128 threads) own one key of the tile
-//   each for the softmax and one value dim per 128-dim band for the epilogue.
+//   the MMAs and owns TMEM; the softmax warps own one key of the tile each
+//   for the softmax and one value dim per 128-dim band for the epilogue, for
+//   32 query rows: warps 2-5 for NR = 32; warps 2-5 (rows 0-31) and 6-9
+//   (rows 32-63) for NR = 64, which halves each thread's softmax work.
 // * Softmax in base 2 with a lazily updated row max: the max moves only when a
 //   new score exceeds it by more than 8 (P <= 2^8, balanced-MLA page, module
 //   overview), and then to 2 below the tile's max (kMaxLead). P enters the PV
@@ -42,6 +44,9 @@ using namespace dec;
 template <int NR>
 struct Cfg {
   static constexpr bool kHiloN = NR == 32;        // hi|lo side by side along N
+  static constexpr int kHalves = NR / 32;         // 128-thread softmax groups of 32 rows
+  static constexpr int kGroup = 128 * kHalves;    // softmax threads
+  static constexpr int kThreads = 64 + kGroup;    // + the TMA warp and the MMA warp
   static constexpr int kQChunk = NR * 128;
   static constexpr int kQBytes = 4 * kQChunk + NR * 64;
   static constexpr int kPBytes = kHiloN ? kTileKeys * 64 : 2 * kTileKeys * 64;
@@ -197,38 +202,40 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
-// Copy one staged 128-dim band of `rows` rows (BF16 out or FP32 partial) to
-// global memory as 16-byte row vectors; the 128 group threads stride the
-// chunks, fully unrolled so the loads pipeline.
-template <int NR, bool DIRECT>
-__device__ __forceinline__ void copy_band(const uint8_t* stage, uint8_t* dst, int rows, int gt) {
-  constexpr int kRowBytes = DIRECT ? 128 * 2 : 128 * 4;
-  constexpr int kCpr = kRowBytes / 16;               // 16-byte chunks per row
-  constexpr long long kPitch = DIRECT ? kDv * 2 : kDv * 4;
-  constexpr int kIters = NR * kCpr / 128;
-  uint4 v[kIters];
-#pragma unroll
-  for (int it = 0; it < kIters; ++it)
-    v[it] = *reinterpret_cast<const uint4*>(stage + (it * 128 + gt) * 16);
-#pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int c = it * 128 + gt, row = c / kCpr, col = c % kCpr;
-    if (row < rows) *reinterpret_cast<uint4*>(dst + row * kPitch + col * 16) = v[it];
-  }
+// The softmax group: one thread per key of the tile and per 32 query rows, so
+// the 64-row kernel runs two 128-thread halves (rows 0-31 and 32-63) on the
+// same keys; each thread always holds 32 rows.
+template <int G>
+__device__ __forceinline__ void group_sync_n() {
+  asm volatile("bar.sync 1, %0;" ::"n"(G) : "memory");
+}
+template <int G>
+__device__ __forceinline__ bool group_any_n(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, 2, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(G)
+      : "memory");
+  return r != 0;
 }
 
 template <int NR>
 __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_t tmem,
                                  int nb) {
   using C = Cfg<NR>;
+  constexpr int G = C::kGroup;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;                   // TMEM lanes this warp may access
   const int tl = quarter * 32 + lane;             // key of the tile / dim of a band
-  const int gt = threadIdx.x - 64;                // 0..127 within the group
+  const int half = C::kHalves == 1 ? 0 : (warp - 2) >> 2;   // which 32 query rows
+  const int r0 = half * 32;
+  const int gt = threadIdx.x - 64;                // 0..G-1 within the group
   const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
   uint32_t g = 0, x = 0;
   bool ok = true;
-  float lp[NR];                                   // this key's share of each row sum
+  float lp[32];                                   // this key's share of its rows' sums
 
   for (uint32_t seq = 0; ok; ++seq) {
     Job jb;
@@ -239,7 +246,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     const int rows = min(NR, a.M - m0);
     if (jb.ntiles == 0) {                          // empty split: out 0, lse -inf
       for (int i = 0; i < rows; ++i)
-        for (int d = gt; d < kDv; d += 128) {
+        for (int d = gt; d < kDv; d += G) {
           if (jb.direct)
             a.out[((long long)jb.r * a.M + m0 + i) * kDv + d] = 0;
           else
@@ -251,48 +258,44 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
       }
       continue;
     }
-    group_sync();                                  // previous job's readers are done
+    group_sync_n<G>();                             // previous job's readers are done
     if (gt < NR) ctl->m_run[gt] = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < NR; ++i) lp[i] = 0.f;
-    group_sync();
+    for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+    group_sync_n<G>();
 
     for (int t = 0; t < jb.ntiles; ++t) {
       const uint32_t gg = g + t;
       const int st = gg & 1;
       if (!(ok = wait_bar(&ctl->s_full[st], (gg >> 1) & 1, ctl, a.status))) break;
       tc::fence_after_sync();
-      float xv[NR];
+      float xv[32];
       {
         uint32_t raw[32];
+        tc::tmem_ld32(tmem + lane_addr + kSCol0 + st * NR + r0, raw);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < NR / 32; ++h) {
-          tc::tmem_ld32(tmem + lane_addr + kSCol0 + st * NR + h * 32, raw);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) xv[h * 32 + i] = __uint_as_float(raw[i]);
-        }
+        for (int i = 0; i < 32; ++i) xv[i] = __uint_as_float(raw[i]);
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&ctl->s_empty[st]);
       const bool valid = jb.j0 + t * kTileKeys + tl < jb.j1;
       bool exceed = false;
 #pragma unroll
-      for (int i = 0; i < NR; ++i) {
+      for (int i = 0; i < 32; ++i) {
         xv[i] = valid ? xv[i] * a.bmm1_log2 : -INFINITY;
-        exceed |= xv[i] > ctl->m_run[i] + 8.f;
+        exceed |= xv[i] > ctl->m_run[r0 + i] + 8.f;
       }
-      if (group_any(exceed)) {
+      if (group_any_n<G>(exceed)) {
         // Rows whose max grew by more than 8: the new max is kMaxLead below the tile's.
-#pragma unroll
-        for (int h = 0; h < NR / 32; ++h) {      // 32 rows at a time: fewer live registers
+        {
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = xv[h * 32 + i];
+          for (int i = 0; i < 32; ++i) v[i] = xv[i];
           transpose_reduce32<true>(v, lane);
-          ctl->red[quarter][h * 32 + lane] = v[0];
+          ctl->red[quarter][r0 + lane] = v[0];
         }
-        group_sync();
+        group_sync_n<G>();
         if (gt < NR) {
           const float tm = fmaxf(fmaxf(ctl->red[0][gt], ctl->red[1][gt]),
                                  fmaxf(ctl->red[2][gt], ctl->red[3][gt]));
@@ -301,27 +304,27 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
           ctl->vec[gt] = mo == -INFINITY ? 0.f : ex2(mo - mn);
           ctl->m_run[gt] = mn;
         }
-        group_sync();
+        group_sync_n<G>();
 #pragma unroll
-        for (int i = 0; i < NR; ++i) lp[i] *= ctl->vec[i];
+        for (int i = 0; i < 32; ++i) lp[i] *= ctl->vec[r0 + i];
         if (t > 0) {
-          // O^T holds tiles < gg: wait for the last PV, then scale its columns.
+          // O^T holds tiles < gg: wait for the last PV, then scale its columns
+          // (32-row kernel: hi and lo columns of the same rows; 64-row kernel:
+          // this half's 32 columns).
           const uint32_t gp = gg - 1;
           if (!(ok = wait_bar(&ctl->pv_done[gp & 1], (gp >> 1) & 1, ctl, a.status))) break;
           tc::fence_after_sync();
 #pragma unroll
           for (int dt = 0; dt < 4; ++dt) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < (C::kHiloN ? 2 : 1); ++h) {
               uint32_t raw[32];
-              const uint32_t addr = tmem + lane_addr + dt * kOCols + h * 32;
+              const uint32_t addr = tmem + lane_addr + dt * kOCols + (C::kHiloN ? h * 32 : r0);
               tc::tmem_ld32(addr, raw);
               tc::tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float f = ctl->vec[C::kHiloN ? i : h * 32 + i];
-                raw[i] = __float_as_uint(__uint_as_float(raw[i]) * f);
-              }
+              for (int i = 0; i < 32; ++i)
+                raw[i] = __float_as_uint(__uint_as_float(raw[i]) * ctl->vec[r0 + i]);
               tc::tmem_st32(addr, raw);
             }
           }
@@ -331,13 +334,13 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
       // P buffer st is free once PV(gg - 2) finished.
       if (gg >= 2 && !(ok = wait_bar(&ctl->pv_done[st], ((gg >> 1) - 1) & 1, ctl, a.status)))
         break;
-      uint32_t hi[NR / 4], lo[NR / 4];
+      uint32_t hi[8], lo[8];
 #pragma unroll
-      for (int i = 0; i < NR; i += 4) {
+      for (int i = 0; i < 32; i += 4) {
         float p[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          p[u] = ex2(xv[i + u] - ctl->m_run[i + u]);
+          p[u] = ex2(xv[i + u] - ctl->m_run[r0 + i + u]);
           lp[i + u] += p[u];
         }
         const uint32_t h01 = f32x2_to_f16x2(p[0], p[1]), h23 = f32x2_to_f16x2(p[2], p[3]);
@@ -348,7 +351,9 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
         lo[i / 4] = (uint32_t)l01 | ((uint32_t)l23 << 16);
       }
       // P^T row of this key, MN-major with the 64-byte swizzle: 16-byte chunk c
-      // of key k lives at k*64 + ((c ^ ((k >> 1) & 3)) * 16).
+      // of key k lives at k*64 + ((c ^ ((k >> 1) & 3)) * 16). 32-row kernel:
+      // chunks 0-1 hold hi, 2-3 lo; 64-row kernel: hi and lo in two planes, this
+      // half's rows in chunks 2 half and 2 half + 1.
       uint8_t* pbuf = smem + C::kOffP + st * C::kPBytes;
       const int sw = (tl >> 1) & 3;
       if constexpr (C::kHiloN) {
@@ -360,17 +365,19 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
       } else {
         uint4* rh = reinterpret_cast<uint4*>(pbuf + tl * 64);
         uint4* rl = reinterpret_cast<uint4*>(pbuf + kTileKeys * 64 + tl * 64);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          rh[c ^ sw] = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-          rl[c ^ sw] = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-        }
+        const int c0 = 2 * half;
+        rh[c0 ^ sw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        rh[(c0 + 1) ^ sw] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        rl[c0 ^ sw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        rl[(c0 + 1) ^ sw] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
       }
       if (!valid) {                                // keys past the split: V rows must be 0
         uint8_t* stage = smem + st * kStageBytes;
+        constexpr int kBands = 4 / C::kHalves;     // each half clears its share of the bands
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4* vrow = reinterpret_cast<uint4*>(stage + c * kChunkBytes + tl * 128);
+        for (int c = 0; c < kBands; ++c) {
+          uint4* vrow =
+              reinterpret_cast<uint4*>(stage + (half * kBands + c) * kChunkBytes + tl * 128);
 #pragma unroll
           for (int u = 0; u < 8; ++u) vrow[u] = make_uint4(0, 0, 0, 0);
         }
@@ -381,81 +388,50 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     if (!ok) break;
 
     // Row sums across the 128 keys of every tile, then 1/l and the LSE.
-#pragma unroll
-    for (int h = 0; h < NR / 32; ++h) {
-      transpose_reduce32<false>(lp + h * 32, lane);
-      ctl->red[quarter][h * 32 + lane] = lp[h * 32];
-    }
-    group_sync();
+    transpose_reduce32<false>(lp, lane);
+    ctl->red[quarter][r0 + lane] = lp[0];
+    group_sync_n<G>();
     if (gt < NR) {
       const float l = ctl->red[0][gt] + ctl->red[1][gt] + ctl->red[2][gt] + ctl->red[3][gt];
       ctl->vec[gt] = l > 0.f ? 1.f / l : 0.f;
       ctl->lse[gt] = l > 0.f ? ctl->m_run[gt] + __log2f(l) : -INFINITY;
     }
-    group_sync();
+    group_sync_n<G>();
     if (!(ok = wait_bar(&ctl->o_full, x & 1, ctl, a.status))) break;
     tc::fence_after_sync();
-    // Each thread holds one output dim of a 128-dim band for every row (TMEM
-    // lane = dim), so for each row the warp's 32 lanes store 32 consecutive
-    // values. With 32 rows they go straight from registers to global memory;
-    // with 64 rows (register-bound) each band is staged through the P buffers
-    // (idle now: the last PV has finished) into 16-byte row vectors.
-    uint8_t* stage = smem + C::kOffP;
-    float sc[NR];                                  // per-row output scale
+    // Each thread holds one output dim of a 128-dim band (TMEM lane = dim) for
+    // its 32 rows, so for each row a warp's 32 lanes store 32 consecutive
+    // values straight from registers.
+    float sc[32];                                  // per-row output scale
 #pragma unroll
-    for (int i = 0; i < NR; ++i) sc[i] = ctl->vec[i] * (jb.direct ? a.bmm2 : 1.f);
+    for (int i = 0; i < 32; ++i) sc[i] = ctl->vec[r0 + i] * (jb.direct ? a.bmm2 : 1.f);
 #pragma unroll 1
     for (int dt = 0; dt < 4; ++dt) {
-      float o[NR];
-      {
-        uint32_t r0[32], r1[32];
-        tc::tmem_ld32(tmem + lane_addr + dt * kOCols, r0);
-        tc::tmem_ld32(tmem + lane_addr + dt * kOCols + 32, r1);
+      float o[32];
+      if constexpr (C::kHiloN) {
+        uint32_t rh[32], rl[32];
+        tc::tmem_ld32(tmem + lane_addr + dt * kOCols, rh);
+        tc::tmem_ld32(tmem + lane_addr + dt * kOCols + 32, rl);
         tc::tmem_wait_ld();
-        if constexpr (C::kHiloN) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            o[i] = __uint_as_float(r0[i]);
-            o[NR - 32 + i] = __uint_as_float(r1[i]);
-          }
-        }
-      }
-      if constexpr (NR == 32) {
-        if (jb.direct) {
-          uint16_t* dst = a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128 + tl;
-#pragma unroll
-          for (int i = 0; i < NR; ++i)
-            if (i < rows) dst[(long long)i * kDv] = f32_to_bf16_bits(o[i] * sc[i]);
-        } else {
-          float* dst = a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128 + tl;
-#pragma unroll
-          for (int i = 0; i < NR; ++i)
-            if (i < rows) dst[(long long)i * kDv] = o[i] * sc[i];
-        }
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(rh[i]) + __uint_as_float(rl[i]);
       } else {
-        if (jb.direct) {
-          uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
+        uint32_t raw[32];
+        tc::tmem_ld32(tmem + lane_addr + dt * kOCols + r0, raw);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < NR; ++i) st16[i * 128 + tl] = f32_to_bf16_bits(o[i] * sc[i]);
-        } else {
-          float* st32 = reinterpret_cast<float*>(stage);
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(raw[i]);
+      }
+      if (jb.direct) {
+        uint16_t* dst = a.out + ((long long)jb.r * a.M + m0 + r0) * kDv + dt * 128 + tl;
 #pragma unroll
-          for (int i = 0; i < NR; ++i) st32[i * 128 + tl] = o[i] * sc[i];
-        }
-        group_sync();
-        if (jb.direct)
-          copy_band<NR, true>(stage, reinterpret_cast<uint8_t*>(
-                                         a.out + ((long long)jb.r * a.M + m0) * kDv + dt * 128),
-                              rows, gt);
-        else
-          copy_band<NR, false>(stage,
-                               reinterpret_cast<uint8_t*>(
-                                   a.part_o + ((long long)jb.item * a.M + m0) * kDv + dt * 128),
-                               rows, gt);
-        group_sync();
+        for (int i = 0; i < 32; ++i)
+          if (r0 + i < rows) dst[(long long)i * kDv] = f32_to_bf16_bits(o[i] * sc[i]);
+      } else {
+        float* dst = a.part_o + ((long long)jb.item * a.M + m0 + r0) * kDv + dt * 128 + tl;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (r0 + i < rows) dst[(long long)i * kDv] = o[i] * sc[i];
       }
     }
     tc::fence_before_sync();
@@ -470,7 +446,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
 }
 
 template <int NR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
 decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
                  const __grid_constant__ CUtensorMap tm_kvr,
                  const __grid_constant__ CUtensorMap tm_q,
@@ -489,17 +465,17 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->s_full[b], 1);
-      tc::mbar_init(&ctl->s_empty[b], 128);
-      tc::mbar_init(&ctl->p_full[b], 128);
+      tc::mbar_init(&ctl->s_empty[b], C::kGroup);
+      tc::mbar_init(&ctl->p_full[b], C::kGroup);
     }
     tc::mbar_init(&ctl->q_full, 1);
     tc::mbar_init(&ctl->q_empty, 1);
     tc::mbar_init(&ctl->o_full, 1);
-    tc::mbar_init(&ctl->o_empty, 128);
+    tc::mbar_init(&ctl->o_empty, C::kGroup);
     tc::mbar_init(&ctl->drain, 1);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->job_full[b], 1);
-      tc::mbar_init(&ctl->job_empty[b], 1 + 128);   // the MMA thread + the softmax group
+      tc::mbar_init(&ctl->job_empty[b], 1 + C::kGroup);   // the MMA thread + the softmax group
     }
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
@@ -569,7 +545,7 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
   const int grid = (int)(jobs < s.num_ctas ? jobs : s.num_ctas);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid > 0 ? grid : 1);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
