@@ -218,12 +218,15 @@ def test_many_splits_of_one_request():
     assert_close(out, lse, ref_o, ref_l, "many splits")
 
 
-@pytest.mark.parametrize("lens,k,H,G", [
-    ((6000,) + (300,) * 30 + (0, 90), 4, 8, 5),     # 32-row kernel, an empty request
-    ((4000, 2500) + (700,) * 12, 7, 8, 7),         # 64-row kernel
-    ((3000, 1500, 400, 64), 2, 64, 3),             # rows-as-M kernel (128 rows, two halves)
+@pytest.mark.parametrize("lens,k,H,G,groups,policy", [
+    ((6000,) + (300,) * 30 + (0, 90), 4, 8, 5, 1, pl.BALANCED),   # 32-row kernel, an empty request
+    ((4000, 2500) + (700,) * 12, 7, 8, 7, 1, pl.BALANCED),       # 64-row kernel
+    ((3000, 1500, 400, 64), 2, 64, 3, 1, pl.BALANCED),           # rows-as-M kernel
+    ((5000, 900, 60) + (400,) * 9, 4, 16, 6, 2, pl.BALANCED),    # row groups, 32-row blocks
+    ((2500, 1800, 0, 700), 2, 64, 4, 2, pl.BALANCED),            # row groups, 64-row blocks
+    ((3000, 100) + (500,) * 6, 4, 8, 3, 1, pl.UNIFORM),          # uniform splits
 ])
-def test_claimed_jobs_and_repeated_decodes_of_one_plan(lens, k, H, G):
+def test_claimed_jobs_and_repeated_decodes_of_one_plan(lens, k, H, G, groups, policy):
     """Far more jobs than CTAs: after its first job a CTA claims the next ones
     in list order from the counters after the items. Three decodes of one plan
     agree bit for bit and with the oracle, and each leaves the work list as the
@@ -231,7 +234,7 @@ def test_claimed_jobs_and_repeated_decodes_of_one_plan(lens, k, H, G):
     b = make_batch_from_lengths(lens, k, H, seed=sum(lens) + G, scaling="amax")
     d = to_device(b)
     eng = mla.FoldedMla(b.R, b.k, b.H, d["bt"].shape[1], d["kv"].shape[0], "cuda", num_ctas=G,
-                        min_split_tokens=64)
+                        min_split_tokens=64, policy=policy, groups=groups)
     bmm1, bmm2 = bmm_scales(b)
     eng.plan(d["lens"])
     torch.cuda.synchronize()
@@ -248,7 +251,7 @@ def test_claimed_jobs_and_repeated_decodes_of_one_plan(lens, k, H, G):
         assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
     ref_o, ref_l = oracle_full(b)
     assert_close(runs[0][0].float().cpu(), runs[0][1].cpu(), ref_o, ref_l,
-                 f"lens={len(lens)} requests k={k} H={H} G={G}")
+                 f"lens={len(lens)} requests k={k} H={H} G={G} groups={groups} policy={policy}")
 
 
 def test_out_of_range_page_sets_status_without_fault():
