@@ -44,7 +44,8 @@ using namespace dec;
 template <int NR>
 struct Cfg {
   static constexpr bool kHiloN = NR == 32;        // hi|lo side by side along N
-  static constexpr int kHalves = NR / 32;         // 128-thread softmax groups of 32 rows
+  static constexpr int kHalves = 2;               // 128-thread softmax groups per row block
+  static constexpr int kRowsPerThread = NR / kHalves;
   static constexpr int kGroup = 128 * kHalves;    // softmax threads
   static constexpr int kThreads = 64 + kGroup;    // + the TMA warp and the MMA warp
   static constexpr int kQChunk = NR * 128;
@@ -72,6 +73,18 @@ __device__ __forceinline__ void tr_step(float* v, int lane, int o) {
     v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
   }
 }
+// The same for v[16] (16 rows per thread): after four halving steps v[0]
+// holds row (lane >> 1) reduced over the 16 lanes that share bit 0 of the
+// lane index; one more exchange with lane ^ 1 completes it.
+template <bool MAX>
+__device__ __forceinline__ void transpose_reduce16(float* v, int lane) {
+  tr_step<16, MAX>(v, lane, 16);
+  tr_step<8, MAX>(v, lane, 8);
+  tr_step<4, MAX>(v, lane, 4);
+  tr_step<2, MAX>(v, lane, 2);
+  const float r = __shfl_xor_sync(0xffffffffu, v[0], 1);
+  v[0] = MAX ? fmaxf(v[0], r) : v[0] + r;
+}
 template <bool MAX>
 __device__ __forceinline__ void transpose_reduce32(float* v, int lane) {
   tr_step<32, MAX>(v, lane, 16);
@@ -79,6 +92,28 @@ __device__ __forceinline__ void transpose_reduce32(float* v, int lane) {
   tr_step<8, MAX>(v, lane, 4);
   tr_step<4, MAX>(v, lane, 2);
   tr_step<2, MAX>(v, lane, 1);
+}
+
+// Reduce this thread's RT row values across the warp's 32 keys and store row
+// results in red[r0 + row] (RT = 32: lane l holds row l; RT = 16: row l >> 1).
+template <int RT, bool MAX>
+__device__ __forceinline__ void reduce_rows(float* v, int lane, float* red_row0) {
+  if constexpr (RT == 32) {
+    transpose_reduce32<MAX>(v, lane);
+    red_row0[lane] = v[0];
+  } else {
+    transpose_reduce16<MAX>(v, lane);
+    if ((lane & 1) == 0) red_row0[lane >> 1] = v[0];
+  }
+}
+// RT consecutive 32-bit TMEM columns of this thread's lane.
+template <int RT>
+__device__ __forceinline__ void tmem_ld_rows(uint32_t taddr, uint32_t (&r)[RT]) {
+  if constexpr (RT == 32) tc::tmem_ld32(taddr, r); else tc::tmem_ld16(taddr, r);
+}
+template <int RT>
+__device__ __forceinline__ void tmem_st_rows(uint32_t taddr, const uint32_t (&r)[RT]) {
+  if constexpr (RT == 32) tc::tmem_st32(taddr, r); else tc::tmem_st16(taddr, r);
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -226,16 +261,17 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
                                  int nb) {
   using C = Cfg<NR>;
   constexpr int G = C::kGroup;
+  constexpr int RT = C::kRowsPerThread;           // 32 or 16
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;                   // TMEM lanes this warp may access
   const int tl = quarter * 32 + lane;             // key of the tile / dim of a band
-  const int half = C::kHalves == 1 ? 0 : (warp - 2) >> 2;   // which 32 query rows
-  const int r0 = half * 32;
+  const int half = C::kHalves == 1 ? 0 : (warp - 2) >> 2;   // which RT query rows
+  const int r0 = half * RT;
   const int gt = threadIdx.x - 64;                // 0..G-1 within the group
   const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
   uint32_t g = 0, x = 0;
   bool ok = true;
-  float lp[32];                                   // this key's share of its rows' sums
+  float lp[RT];                                   // this key's share of its rows' sums
 
   for (uint32_t seq = 0; ok; ++seq) {
     Job jb;
@@ -261,7 +297,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     group_sync_n<G>();                             // previous job's readers are done
     if (gt < NR) ctl->m_run[gt] = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+    for (int i = 0; i < RT; ++i) lp[i] = 0.f;
     group_sync_n<G>();
 
     for (int t = 0; t < jb.ntiles; ++t) {
@@ -269,31 +305,30 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
       const int st = gg & 1;
       if (!(ok = wait_bar(&ctl->s_full[st], (gg >> 1) & 1, ctl, a.status))) break;
       tc::fence_after_sync();
-      float xv[32];
+      float xv[RT];
       {
-        uint32_t raw[32];
-        tc::tmem_ld32(tmem + lane_addr + kSCol0 + st * NR + r0, raw);
+        uint32_t raw[RT];
+        tmem_ld_rows<RT>(tmem + lane_addr + kSCol0 + st * NR + r0, raw);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] = __uint_as_float(raw[i]);
+        for (int i = 0; i < RT; ++i) xv[i] = __uint_as_float(raw[i]);
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&ctl->s_empty[st]);
       const bool valid = jb.j0 + t * kTileKeys + tl < jb.j1;
       bool exceed = false;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < RT; ++i) {
         xv[i] = valid ? xv[i] * a.bmm1_log2 : -INFINITY;
         exceed |= xv[i] > ctl->m_run[r0 + i] + 8.f;
       }
       if (group_any_n<G>(exceed)) {
         // Rows whose max grew by more than 8: the new max is kMaxLead below the tile's.
         {
-          float v[32];
+          float v[RT];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = xv[i];
-          transpose_reduce32<true>(v, lane);
-          ctl->red[quarter][r0 + lane] = v[0];
+          for (int i = 0; i < RT; ++i) v[i] = xv[i];
+          reduce_rows<RT, true>(v, lane, &ctl->red[quarter][r0]);
         }
         group_sync_n<G>();
         if (gt < NR) {
@@ -306,11 +341,11 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
         }
         group_sync_n<G>();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) lp[i] *= ctl->vec[r0 + i];
+        for (int i = 0; i < RT; ++i) lp[i] *= ctl->vec[r0 + i];
         if (t > 0) {
-          // O^T holds tiles < gg: wait for the last PV, then scale its columns
-          // (32-row kernel: hi and lo columns of the same rows; 64-row kernel:
-          // this half's 32 columns).
+          // O^T holds tiles < gg: wait for the last PV, then scale this
+          // thread's rows' columns (32-row kernel: in both the hi and the lo
+          // columns).
           const uint32_t gp = gg - 1;
           if (!(ok = wait_bar(&ctl->pv_done[gp & 1], (gp >> 1) & 1, ctl, a.status))) break;
           tc::fence_after_sync();
@@ -318,14 +353,14 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
           for (int dt = 0; dt < 4; ++dt) {
 #pragma unroll
             for (int h = 0; h < (C::kHiloN ? 2 : 1); ++h) {
-              uint32_t raw[32];
-              const uint32_t addr = tmem + lane_addr + dt * kOCols + (C::kHiloN ? h * 32 : r0);
-              tc::tmem_ld32(addr, raw);
+              uint32_t raw[RT];
+              const uint32_t addr = tmem + lane_addr + dt * kOCols + h * 32 + r0;
+              tmem_ld_rows<RT>(addr, raw);
               tc::tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
+              for (int i = 0; i < RT; ++i)
                 raw[i] = __float_as_uint(__uint_as_float(raw[i]) * ctl->vec[r0 + i]);
-              tc::tmem_st32(addr, raw);
+              tmem_st_rows<RT>(addr, raw);
             }
           }
           tc::tmem_wait_st();
@@ -334,9 +369,9 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
       // P buffer st is free once PV(gg - 2) finished.
       if (gg >= 2 && !(ok = wait_bar(&ctl->pv_done[st], ((gg >> 1) - 1) & 1, ctl, a.status)))
         break;
-      uint32_t hi[8], lo[8];
+      uint32_t hi[RT / 4], lo[RT / 4];
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
+      for (int i = 0; i < RT; i += 4) {
         float p[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -351,25 +386,21 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
         lo[i / 4] = (uint32_t)l01 | ((uint32_t)l23 << 16);
       }
       // P^T row of this key, MN-major with the 64-byte swizzle: 16-byte chunk c
-      // of key k lives at k*64 + ((c ^ ((k >> 1) & 3)) * 16). 32-row kernel:
-      // chunks 0-1 hold hi, 2-3 lo; 64-row kernel: hi and lo in two planes, this
-      // half's rows in chunks 2 half and 2 half + 1.
+      // (16 rows) of key k lives at k*64 + ((c ^ ((k >> 1) & 3)) * 16). 32-row
+      // kernel: chunks 0-1 hold hi, 2-3 lo; 64-row kernel: hi and lo in two
+      // planes. This thread writes the chunks of its rows r0 .. r0 + RT - 1.
       uint8_t* pbuf = smem + C::kOffP + st * C::kPBytes;
       const int sw = (tl >> 1) & 3;
-      if constexpr (C::kHiloN) {
-        uint4* row = reinterpret_cast<uint4*>(pbuf + tl * 64);
-        row[0 ^ sw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        row[1 ^ sw] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        row[2 ^ sw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        row[3 ^ sw] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-      } else {
-        uint4* rh = reinterpret_cast<uint4*>(pbuf + tl * 64);
-        uint4* rl = reinterpret_cast<uint4*>(pbuf + kTileKeys * 64 + tl * 64);
-        const int c0 = 2 * half;
-        rh[c0 ^ sw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        rh[(c0 + 1) ^ sw] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        rl[c0 ^ sw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        rl[(c0 + 1) ^ sw] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+      const int cb = r0 / 16;
+      uint4* rh = reinterpret_cast<uint4*>(pbuf + tl * 64);
+      uint4* rl = C::kHiloN ? rh + 2 : reinterpret_cast<uint4*>(pbuf + kTileKeys * 64 + tl * 64);
+#pragma unroll
+      for (int j = 0; j < RT / 16; ++j) {
+        const int ch = C::kHiloN ? (cb + j) ^ sw : (cb + j) ^ sw;
+        const int cl = C::kHiloN ? (2 + cb + j) ^ sw : (cb + j) ^ sw;
+        rh[ch] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+        (C::kHiloN ? rh : rl)[cl] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2],
+                                                lo[4 * j + 3]);
       }
       if (!valid) {                                // keys past the split: V rows must be 0
         uint8_t* stage = smem + st * kStageBytes;
@@ -388,8 +419,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     if (!ok) break;
 
     // Row sums across the 128 keys of every tile, then 1/l and the LSE.
-    transpose_reduce32<false>(lp, lane);
-    ctl->red[quarter][r0 + lane] = lp[0];
+    reduce_rows<RT, false>(lp, lane, &ctl->red[quarter][r0]);
     group_sync_n<G>();
     if (gt < NR) {
       const float l = ctl->red[0][gt] + ctl->red[1][gt] + ctl->red[2][gt] + ctl->red[3][gt];
@@ -400,37 +430,37 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     if (!(ok = wait_bar(&ctl->o_full, x & 1, ctl, a.status))) break;
     tc::fence_after_sync();
     // Each thread holds one output dim of a 128-dim band (TMEM lane = dim) for
-    // its 32 rows, so for each row a warp's 32 lanes store 32 consecutive
+    // its RT rows, so for each row a warp's 32 lanes store 32 consecutive
     // values straight from registers.
-    float sc[32];                                  // per-row output scale
+    float sc[RT];                                  // per-row output scale
 #pragma unroll
-    for (int i = 0; i < 32; ++i) sc[i] = ctl->vec[r0 + i] * (jb.direct ? a.bmm2 : 1.f);
+    for (int i = 0; i < RT; ++i) sc[i] = ctl->vec[r0 + i] * (jb.direct ? a.bmm2 : 1.f);
 #pragma unroll 1
     for (int dt = 0; dt < 4; ++dt) {
-      float o[32];
+      float o[RT];
       if constexpr (C::kHiloN) {
-        uint32_t rh[32], rl[32];
-        tc::tmem_ld32(tmem + lane_addr + dt * kOCols, rh);
-        tc::tmem_ld32(tmem + lane_addr + dt * kOCols + 32, rl);
+        uint32_t rh[RT], rl[RT];
+        tmem_ld_rows<RT>(tmem + lane_addr + dt * kOCols + r0, rh);
+        tmem_ld_rows<RT>(tmem + lane_addr + dt * kOCols + 32 + r0, rl);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(rh[i]) + __uint_as_float(rl[i]);
+        for (int i = 0; i < RT; ++i) o[i] = __uint_as_float(rh[i]) + __uint_as_float(rl[i]);
       } else {
-        uint32_t raw[32];
-        tc::tmem_ld32(tmem + lane_addr + dt * kOCols + r0, raw);
+        uint32_t raw[RT];
+        tmem_ld_rows<RT>(tmem + lane_addr + dt * kOCols + r0, raw);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(raw[i]);
+        for (int i = 0; i < RT; ++i) o[i] = __uint_as_float(raw[i]);
       }
       if (jb.direct) {
         uint16_t* dst = a.out + ((long long)jb.r * a.M + m0 + r0) * kDv + dt * 128 + tl;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < RT; ++i)
           if (r0 + i < rows) dst[(long long)i * kDv] = f32_to_bf16_bits(o[i] * sc[i]);
       } else {
         float* dst = a.part_o + ((long long)jb.item * a.M + m0 + r0) * kDv + dt * 128 + tl;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < RT; ++i)
           if (r0 + i < rows) dst[(long long)i * kDv] = o[i] * sc[i];
       }
     }
