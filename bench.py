@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -179,13 +180,25 @@ def algorithmic_bytes(lens, M: int) -> int:
     return int(D_QK * lens.sum() + len(lens) * M * (D_QK + 512 * 2 + 4) + 4 * pages.sum())
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def strip_comments(text: str) -> str:
+    """C/C++ source without its comments and trailing blanks (the decode
+    sources hold no string literal containing a comment marker)."""
+    text = _COMMENT.sub("", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_hash() -> str:
+    """Hash of the decode kernels' code, comments excluded: an ncu capture
+    stays valid for the source it was taken on whatever its comments say."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_folded_gb300", "csrc")
     for name in DECODE_SOURCES:
         path = os.path.join(csrc, name)
         if os.path.exists(path):
-            h.update(open(path, "rb").read())
+            h.update(strip_comments(open(path).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -20,10 +20,10 @@
 //                          the same shared-memory tile, read MN-major)
 // * Warp roles: warp 0 issues TMA (per-page gathers through the block table
 //   into a 2-stage ring of 128-key tiles; Q block once per job); warp 1 issues
-//   the MMAs and owns TMEM; the softmax warps own one key of the tile each
-//   for the softmax and one value dim per 128-dim band for the epilogue, for
-//   32 query rows: warps 2-5 for NR = 32; warps 2-5 (rows 0-31) and 6-9
-//   (rows 32-63) for NR = 64, which halves each thread's softmax work.
+//   the MMAs and owns TMEM; warps 2-9 (two 128-thread halves) own one key of
+//   the tile each for the softmax and one value dim per 128-dim band for the
+//   epilogue, the first half for query rows 0 .. NR/2 - 1 and the second for
+//   the rest (16 rows per thread for NR = 32, 32 for NR = 64).
 // * Softmax in base 2 with a lazily updated row max: the max moves only when a
 //   new score exceeds it by more than 8 (P <= 2^8, balanced-MLA page, module
 //   overview), and then to 2 below the tile's max (kMaxLead). P enters the PV
@@ -237,9 +237,8 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
-// The softmax group: one thread per key of the tile and per 32 query rows, so
-// the 64-row kernel runs two 128-thread halves (rows 0-31 and 32-63) on the
-// same keys; each thread always holds 32 rows.
+// The softmax group: two 128-thread halves on the same keys, one thread per
+// key of the tile and per NR/2 query rows (16 or 32 rows per thread).
 template <int G>
 __device__ __forceinline__ void group_sync_n() {
   asm volatile("bar.sync 1, %0;" ::"n"(G) : "memory");

@@ -47,3 +47,12 @@ def test_roofline_picks_binding_bound():
     assert hi["bound"] == "tensor" and hi["unit"] == "TFLOP/s"
     assert hi["frac"] == pytest.approx(hi["achieved"] / fp8)
     assert bench.algorithmic_flops([100, 28], 3) == 2 * 3 * 1088 * 128
+
+
+def test_source_hash_ignores_comments_only():
+    code = "int f(int a) {\n  return a + 1;  // one more\n}\n"
+    commented = "/* a note\n   over lines */\nint f(int a) {\n  // first\n  return a + 1;\n}\n"
+    changed = "int f(int a) {\n  return a + 2;  // one more\n}\n"
+    assert bench.strip_comments(code) == bench.strip_comments(commented)
+    assert bench.strip_comments(code) != bench.strip_comments(changed)
+    assert len(bench.source_hash()) == 16
