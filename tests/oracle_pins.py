@@ -11,7 +11,8 @@ Pins used (none re-types the oracle's own expression):
 * closed forms: one key; zero query (uniform weights); identical keys;
   one dominant key;
 * library special case: float64 torch.softmax(S) @ V on one contiguous page;
-* invariants: fold == unfold row by row, split-merge invariance, convexity.
+* invariants: fold == unfold row by row, split-merge invariance, convexity;
+* the per-row sampler against the brute force and the whole-batch oracle.
 """
 from __future__ import annotations
 
@@ -237,8 +238,48 @@ def check_convexity():
     return fails
 
 
+def _row_picks(R, M, n, rng):
+    """(request, folded row) picks: the first and last row of every request
+    plus n random ones."""
+    picks = [(r, 0) for r in range(R)] + [(r, M - 1) for r in range(R)]
+    picks += [(int(rng.integers(R)), int(rng.integers(M))) for _ in range(n)]
+    return picks
+
+
+def check_row_sampler(cases=TINY_CASES, seed=71):
+    """The per-row sampler the full-size GPU checks use as ground truth: every
+    pick (request r, folded row m = t*H + h) equals the brute force's row for
+    token r*k + t, head h (drafter-attention page, module overview: rows run
+    token-major, then head), and the whole-batch oracle's row on a batch with
+    k and H both above one."""
+    fails = []
+    rng = np.random.default_rng(seed)
+    for case in cases:
+        b, (o_ref, l_ref) = _tiny(case)
+        M = b.k * b.H
+        picks = _row_picks(b.R, M, 12, rng)
+        o, l = att.mla_decode_rows(b.q.numpy(), b.kv.numpy(), b.block_table.numpy(),
+                                   b.seq_lens.numpy(), b.k, b.sm_scale, b.q_scale, b.kv_scale,
+                                   picks)
+        for i, (r, m) in enumerate(picks):
+            t, h = r * b.k + m // b.H, m % b.H
+            _cmp(f"rows bf out {case[0]} pick {(r, m)}", o[i], o_ref[t, h], 1e-12, fails)
+            _cmp(f"rows bf lse {case[0]} pick {(r, m)}", l[i], l_ref[t, h], 1e-12, fails)
+    b = make_batch_from_lengths((200, 70, 1), 3, 5, seed=seed, extra_pages=1)
+    o_all, l_all = run_oracle(b)
+    M = b.k * b.H
+    picks = _row_picks(b.R, M, 20, rng)
+    o, l = att.mla_decode_rows(b.q.numpy(), b.kv.numpy(), b.block_table.numpy(),
+                               b.seq_lens.numpy(), b.k, b.sm_scale, b.q_scale, b.kv_scale, picks)
+    for i, (r, m) in enumerate(picks):
+        t, h = r * b.k + m // b.H, m % b.H
+        _cmp(f"rows out pick {(r, m)}", o[i], o_all[t, h], 1e-12, fails)
+        _cmp(f"rows lse pick {(r, m)}", l[i], l_all[t, h], 1e-12, fails)
+    return fails
+
+
 ALL_CHECKS = (check_brute_force, check_closed_forms, check_library_softmax,
-              check_fold_equals_unfold, check_split_merge, check_convexity)
+              check_fold_equals_unfold, check_split_merge, check_convexity, check_row_sampler)
 
 
 def all_failures():

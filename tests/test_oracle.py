@@ -57,6 +57,10 @@ def test_convexity():
     assert pins.check_convexity() == []
 
 
+def test_row_sampler_matches_brute_force_and_whole_batch():
+    assert pins.check_row_sampler() == []
+
+
 def test_merge_empty_and_single():
     o = np.random.default_rng(0).standard_normal((3, 4, 8))
     l = np.full((3, 4), -np.inf)

@@ -54,6 +54,28 @@ def _head_major_decode(*a, **kw):
     return o.reshape(rows, H, 512), l.reshape(rows, H)
 
 
+def _rows_variant(split_by_k=False, no_request_offset=False):
+    """mla_decode_rows with one index mistake."""
+    def mla_decode_rows(q_codes, kv_codes, block_table, seq_lens, tokens_per_request,
+                        sm_scale, q_scale, kv_scale, picks):
+        q = np.asarray(q_codes)
+        _, H, _ = q.shape
+        k = int(tokens_per_request)
+        outs, lses = [], []
+        for r, m in picks:
+            t, h = divmod(int(m), k if split_by_k else H)
+            t, h = min(t, k - 1), min(h, H - 1)
+            row = t if no_request_offset else r * k + t
+            kd = att.request_keys(kv_codes, np.asarray(block_table)[r], 0,
+                                  int(np.asarray(seq_lens)[r]), kv_scale)
+            qd = att.e4m3.decode(q[row, h][None, :]) * float(q_scale)
+            o, l2 = att.attend(qd, kd, sm_scale)
+            outs.append(o[0])
+            lses.append(l2[0])
+        return np.stack(outs), np.array(lses)
+    return mla_decode_rows
+
+
 def _combine_natural(o, l):
     o = np.asarray(o); l = np.asarray(l)
     mx = l.max(axis=0)
@@ -73,6 +95,9 @@ MUTANTS = {
     "one key past the length": ("request_keys", _keys_variant(extra=1)),
     "head-major row order": ("mla_decode", _head_major_decode),
     "merge weights in base e": ("combine", _combine_natural),
+    "row sampler splits rows by k": ("mla_decode_rows", _rows_variant(split_by_k=True)),
+    "row sampler drops the request offset": ("mla_decode_rows",
+                                             _rows_variant(no_request_offset=True)),
 }
 
 
