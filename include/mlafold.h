@@ -167,6 +167,26 @@ int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
                           size_t workspace_bytes, void *out, float *lse, int32_t *status,
                           mla_stream_t stream);
 
+/* Failure detection, for tests: mla_folded_decode with every pipeline wait
+ * bounded by wait_limit_ns (1 ms .. 2 s; the regular call uses 2 s) and with
+ * the first KV tile copy of CTA 0 never issued, so that a wait on it runs out
+ * (the DSA prepared-layers page, `held`, records a CUDA graph that hung when a
+ * kernel read its inputs before its dependency wait; every wait here is
+ * bounded instead, so a lost input stops the CTA). The CTA then ORs
+ * MLA_FAULT_WAIT_TIMEOUT into *status (required here), stops, lets its copies
+ * and MMAs in flight finish, frees its tensor memory and returns; the other
+ * CTAs finish the rest of the plan, and the job counters in `work` are back at
+ * their planned state afterwards, so a regular decode of the same plan may
+ * follow. The jobs the stopped CTA had taken are not computed: `out`, `lse`
+ * and the workspace hold unspecified values for them. No trap, no fault. */
+int32_t mla_folded_decode_wait_test(const mla_shape *shape, const void *q, const void *kv,
+                                    const int32_t *block_table, const int32_t *seq_lens,
+                                    float bmm1_scale, float bmm2_scale, const int32_t *counts,
+                                    int32_t *work, int32_t list_len, void *workspace,
+                                    size_t workspace_bytes, void *out, float *lse,
+                                    int32_t *status, uint64_t wait_limit_ns,
+                                    mla_stream_t stream);
+
 /* LSE reduction of the split partials into `out` and `lse` for the requests
  * with two or more splits: out = bmm2_scale * sum_s w_s O_s / sum_s w_s, with
  * w_s = 2^(lse_s - max_s lse_s), rounded once to BF16; lse = max + log2 sum w
@@ -220,6 +240,43 @@ int32_t mla_uv_combine(const mla_shape *shape, const int32_t *counts, const int3
 int32_t mla_lse_merge(int32_t S, int32_t rows, const void *parts_out, const float *parts_lse,
                       void *out, float *lse, mla_stream_t stream);
 
+/* The tiered launch (drafter-attention page, `balanced_decode`): instead of
+ * one persistent decode over a device-balanced plan, the longest decode rows
+ * move out of one unsplit launch into "tiers" of a few rows each, every tier a
+ * decode launch of its own whose rows are split, on streams of lower priority.
+ * The two calls below are its data steps; the launches themselves are plain
+ * mla_plan_splits / mla_folded_decode / mla_split_combine calls.
+ *
+ * mla_tier_plan -- which rows move (drafter-attention page, `_balanced_tables`
+ * and `_plan_kernel`), one CTA on the device: rank the `rows` decode rows by
+ * length, longest first (ties: lower row first); a row of rank r < split_rows
+ * moves when len * move_den * pairs > move_num * sum(len) ("longer than MOVE
+ * of a pair's share of the batch's keys").
+ *   seq_lens   [rows] int32, device (negative is read as 0).
+ *   rest_lens  [rows] int32, device, written: each row's length in the
+ *              unsplit launch, 0 for a moved row.
+ *   tier_rows  [split_rows] int32, device, written: the batch row of rank r
+ *              if it moved, else `rows`.
+ *   tier_lens  [split_rows] int32, device, written: its length if it moved,
+ *              else 0.
+ *   1 <= rows <= 1024, 0 <= split_rows <= rows, 1 <= pairs <= 4096,
+ *   1 <= move_num, move_den <= 65536. Integer arithmetic only; the project's
+ *   CPU rule reproduces it bit for bit. */
+int32_t mla_tier_plan(int32_t rows, int32_t split_rows, int32_t pairs, int32_t move_num,
+                      int32_t move_den, const int32_t *seq_lens, int32_t *rest_lens,
+                      int32_t *tier_rows, int32_t *tier_lens, mla_stream_t stream);
+
+/* mla_row_copy -- whole rows of `row_bytes` bytes (a multiple of 4) between
+ * two row-major buffers, for the target rows whose index lies in [0, bound)
+ * (drafter-attention page, `_row_copy_kernel`): with gather = 1 dst row i
+ * receives src row index[i]; with gather = 0 src row i goes to dst row
+ * index[i]. i runs over 0 .. targets-1; other rows are not touched.
+ *   src, dst: device, 4-byte aligned (16-byte aligned rows copy in 16-byte
+ *   pieces); gather: src holds `bound` rows, dst `targets`; scatter: the
+ *   reverse. index [targets] int32, device. targets = 0 launches nothing. */
+int32_t mla_row_copy(const void *src, void *dst, const int32_t *index, int32_t targets,
+                     int32_t bound, int64_t row_bytes, int32_t gather, mla_stream_t stream);
+
 /* The decode of mla_folded_decode followed by mla_split_combine, for callers
  * that cannot allocate device memory (a host application or plugin whose
  * allocator owns the device, or code running while a memory pool is sized):
@@ -229,13 +286,18 @@ int32_t mla_lse_merge(int32_t S, int32_t rows, const void *parts_out, const floa
  * on that GPU until the process exits. The pages have no counterpart; it is
  * an addition of this library.
  *   Arguments, layouts and results are those of mla_folded_decode (which also
- *   writes the multi-split rows here, as mla_split_combine would).
+ *   writes the multi-split rows here, as mla_split_combine would); the plan
+ *   (counts, work) comes from mla_plan_splits as usual.
  *   Returns MLA_ERR_SCRATCH_LIMIT, launching nothing, when
  *   mla_workspace_bytes(shape) exceeds MLA_NOALLOC_SCRATCH_BYTES.
  *   Calls no cudaMalloc, cudaFree or other allocating routine.
  *   The first call on a device looks the array's device address up
- *   (cudaGetSymbolAddress) with that device current and caches it; make that
- *   first call before any stream capture.
+ *   (cudaGetSymbolAddress) with that device current and caches it. With the
+ *   CUDA runtime's lazy module loading that first lookup is also when the
+ *   64 MiB are committed on the device, so make the first call (a warm-up
+ *   will do) before sizing memory pools and before any stream capture. The
+ *   cached address does not survive cudaDeviceReset: do not call this entry
+ *   point on a device after resetting it in the same process.
  *   Every call on a device uses the same array: two calls whose work overlaps
  *   on the GPU (different streams, no ordering between them) race and corrupt
  *   each other's results. Nothing in the array needs clearing between calls. */

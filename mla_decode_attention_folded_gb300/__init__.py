@@ -28,7 +28,9 @@ from ._lib import (FAULT_PAGE_RANGE, FAULT_WAIT_TIMEOUT, FAULT_WORK_ITEM, MlaErr
 
 __all__ = ["MlaShape", "MlaError", "POLICY_BALANCED", "POLICY_UNIFORM", "make_shape",
            "plan_list_len", "workspace_bytes", "plan_splits", "folded_decode",
-           "split_combine", "uv_combine", "lse_merge", "folded_decode_noalloc", "FoldedMla", "fold_factor", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
+           "split_combine", "uv_combine", "lse_merge", "folded_decode_noalloc",
+           "folded_decode_wait_test", "tier_plan", "row_copy", "balanced_tiers", "TIERS", "MOVE",
+           "FoldedMla", "TieredMla", "fold_factor", "FAULT_WAIT_TIMEOUT", "FAULT_PAGE_RANGE",
            "FAULT_WORK_ITEM", "library_path"]
 
 PAGE = 64
@@ -97,6 +99,20 @@ def folded_decode(shape: MlaShape, q, kv, block_table, seq_lens, bmm1_scale: flo
         _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))
 
 
+def folded_decode_wait_test(shape: MlaShape, q, kv, block_table, seq_lens, bmm1_scale: float,
+                            bmm2_scale: float, counts, work, workspace, out, lse, status,
+                            wait_limit_ns: int, stream=None) -> None:
+    """Failure-detection test hook: the decode with every pipeline wait bounded
+    by wait_limit_ns and CTA 0's first KV copy withheld, so that a wait runs
+    out and MLA_FAULT_WAIT_TIMEOUT is set in `status` (see include/mlafold.h)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.check("mla_folded_decode_wait_test", _lib.load().mla_folded_decode_wait_test(
+        ctypes.byref(shape), _ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens),
+        float(bmm1_scale), float(bmm2_scale), _ptr(counts), _ptr(work), work.numel(),
+        _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), _ptr(status), int(wait_limit_ns),
+        _stream(stream)))
+
+
 def split_combine(shape: MlaShape, counts, work, workspace, bmm2_scale: float, out, lse,
                   stream=None) -> None:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -137,6 +153,48 @@ def folded_decode_noalloc(shape: MlaShape, q, kv, block_table, seq_lens, bmm1_sc
         ctypes.byref(shape), _ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens),
         float(bmm1_scale), float(bmm2_scale), _ptr(counts), _ptr(work), work.numel(), _ptr(out),
         _ptr(lse), _ptr(status), _stream(stream)))
+
+
+# The tiered launch's constants. The pages name TIERS and MOVE without values
+# (drafter-attention page, `balanced_tiers`, `_balanced_tables`); these are
+# this library's: tiers of 8, 16 and 32 rows, and a row moves when it is longer
+# than one pair's share of the batch's keys.
+TIERS = (8, 16, 32)
+MOVE = (1, 1)
+
+
+def balanced_tiers(rows: int, sms: int, tiers=TIERS) -> tuple:
+    """Tier sizes for `rows` decode rows on `sms` SMs (drafter-attention page,
+    `balanced_tiers`): none when rows * 4 <= sms, else the sizes of `tiers` in
+    order while their sum stays at most rows // 2."""
+    if rows * 4 <= sms:
+        return ()
+    out: list = []
+    for size in tiers:
+        if sum(out) + size > rows // 2:
+            break
+        out.append(size)
+    return tuple(out)
+
+
+def tier_plan(rows: int, split_rows: int, pairs: int, move, seq_lens, rest_lens, tier_rows,
+              tier_lens, stream=None) -> None:
+    """Which rows move into the tiers (see mla_tier_plan in include/mlafold.h)."""
+    _lib.check("mla_tier_plan", _lib.load().mla_tier_plan(
+        rows, split_rows, pairs, int(move[0]), int(move[1]), _ptr(seq_lens), _ptr(rest_lens),
+        _ptr(tier_rows), _ptr(tier_lens), _stream(stream)))
+
+
+def row_copy(src, dst, index, targets: int, bound: int, gather: bool, stream=None) -> None:
+    """Whole-row gather (dst[i] = src[index[i]]) or scatter (dst[index[i]] =
+    src[i]) of the rows whose index lies in [0, bound); rows are the leading
+    dimension of src and dst (see mla_row_copy in include/mlafold.h)."""
+    row_bytes = src[0].numel() * src.element_size()
+    if dst[0].numel() * dst.element_size() != row_bytes:
+        raise ValueError("src and dst rows differ in size")
+    _lib.check("mla_row_copy", _lib.load().mla_row_copy(
+        _ptr(src), _ptr(dst), _ptr(index), int(targets), int(bound), int(row_bytes),
+        1 if gather else 0, _stream(stream)))
 
 
 class FoldedMla:
@@ -200,3 +258,89 @@ class FoldedMla:
         uv_combine(self.shape, self.counts, self.work, self.workspace, bmm2_scale, out, w_uv, y,
                    self.status, stream)
         return y
+
+
+class TieredMla:
+    """The pages' tiered launch (drafter-attention page, `balanced_decode`),
+    built from this library's kernels for comparison with the single
+    persistent decode of `FoldedMla`: the longest decode rows move out of one
+    unsplit launch into tiers of TIERS rows, each tier a decode launch of its
+    own with split rows, on streams of decreasing priority (the unsplit launch
+    on the highest, then the tiers from the coarsest split to the finest).
+
+    One folded decode row per request (groups = 1). Split counts: the unsplit
+    launch gives every row one split; a tier of m rows gets this library's
+    uniform split count for m rows (the pages' stock kernel gives sms // (2m)
+    splits: CTA pairs per row split; here the plan's concurrent items per row).
+    Every buffer is allocated here, before any capture."""
+
+    def __init__(self, R: int, k: int, H: int, max_pages: int, num_pages: int, device=None,
+                 sms: int | None = None, tiers=None, move=MOVE):
+        self.device = torch.device(device if device is not None else "cuda")
+        if sms is None:
+            sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self.R, self.k, self.H, self.M, self.max_pages = R, k, H, k * H, max_pages
+        self.tiers = balanced_tiers(R, sms) if tiers is None else tuple(tiers)
+        self.split_rows = sum(self.tiers)
+        if self.split_rows > R:
+            raise ValueError("the tiers hold more rows than the batch")
+        self.pairs = max(1, sms // 2)
+        self.move = tuple(move)
+        self.unsplit = FoldedMla(R, k, H, max_pages, num_pages, self.device, num_ctas=sms,
+                                 max_splits=1, policy=POLICY_UNIFORM)
+        self.engines = [FoldedMla(m, k, H, max_pages, num_pages, self.device, num_ctas=sms,
+                                  policy=POLICY_UNIFORM) for m in self.tiers]
+        n = max(self.split_rows, 1)
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.rest = torch.zeros(R, **i32)
+        self.tier_rows = torch.full((n,), R, **i32)
+        self.tier_lens = torch.zeros(n, **i32)
+        self.q_s = torch.empty((n * k, H, 576), dtype=torch.uint8, device=self.device)
+        self.bt_s = torch.zeros((n, max_pages), **i32)
+        self.out_s = torch.empty((n, self.M, 512), dtype=torch.bfloat16, device=self.device)
+        self.lse_s = torch.empty((n, self.M), dtype=torch.float32, device=self.device)
+        low, high = torch.cuda.Stream.priority_range()
+        self.streams = [torch.cuda.Stream(self.device, priority=min(low, high + i))
+                        for i in range(len(self.tiers) + 1)]
+
+    def decode(self, q, kv, block_table, seq_lens, bmm1_scale: float, bmm2_scale: float,
+               out=None, lse=None, return_lse: bool = True):
+        """out [R, M, 512] BF16 and the base-2 lse [R, M] (None without
+        return_lse), as FoldedMla.decode returns them."""
+        if out is None:
+            out = torch.empty((self.R, self.M, 512), dtype=torch.bfloat16, device=self.device)
+        if lse is None and return_lse:
+            lse = torch.empty((self.R, self.M), dtype=torch.float32, device=self.device)
+        if not return_lse:
+            lse = None
+        main = torch.cuda.current_stream(self.device)
+        R, k, n = self.R, self.k, self.split_rows
+        tier_plan(R, n, self.pairs, self.move, seq_lens, self.rest, self.tier_rows,
+                  self.tier_lens, main)
+        first = self.streams[0]
+        first.wait_stream(main)
+        self.unsplit.plan(self.rest, first)
+        self.unsplit.decode(q, kv, block_table, self.rest, bmm1_scale, bmm2_scale, out=out,
+                            lse=lse, stream=first, return_lse=return_lse)
+        if n:
+            row_copy(q.view(R, -1), self.q_s.view(n, -1), self.tier_rows, n, R, True, main)
+            row_copy(block_table, self.bt_s, self.tier_rows, n, R, True, main)
+            launches, start = [], 0
+            for m, eng in zip(self.tiers, self.engines):
+                launches.append((start, m, eng))
+                start += m
+            for stream, (b, m, eng) in zip(self.streams[1:], reversed(launches)):
+                stream.wait_stream(main)
+                lens = self.tier_lens[b:b + m]
+                eng.plan(lens, stream)
+                eng.decode(self.q_s[b * k:(b + m) * k], kv, self.bt_s[b:b + m], lens, bmm1_scale,
+                           bmm2_scale, out=self.out_s[b:b + m],
+                           lse=self.lse_s[b:b + m] if return_lse else None, stream=stream,
+                           return_lse=return_lse)
+        for stream in self.streams:
+            main.wait_stream(stream)
+        if n:
+            row_copy(self.out_s, out, self.tier_rows, n, R, False, main)
+            if lse is not None:
+                row_copy(self.lse_s, lse, self.tier_rows, n, R, False, main)
+        return out, lse

@@ -21,7 +21,8 @@ FAULT_WAIT_TIMEOUT, FAULT_PAGE_RANGE, FAULT_WORK_ITEM = 0x1, 0x2, 0x4
 # Every symbol include/mlafold.h declares.
 EXPORTS = ("mla_plan_list_len", "mla_workspace_bytes", "mla_plan_splits",
            "mla_folded_decode", "mla_split_combine", "mla_lse_merge",
-           "mla_folded_decode_noalloc", "mla_uv_combine")
+           "mla_folded_decode_noalloc", "mla_uv_combine", "mla_folded_decode_wait_test",
+           "mla_tier_plan", "mla_row_copy")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -60,6 +61,13 @@ def load() -> ctypes.CDLL:
     lib.mla_plan_splits.restype = I32
     lib.mla_folded_decode.argtypes = [SP, P, P, P, P, F, F, P, P, I32, P, SZ, P, P, P, P]
     lib.mla_folded_decode.restype = I32
+    lib.mla_folded_decode_wait_test.argtypes = [SP, P, P, P, P, F, F, P, P, I32, P, SZ, P, P, P,
+                                                ctypes.c_uint64, P]
+    lib.mla_folded_decode_wait_test.restype = I32
+    lib.mla_tier_plan.argtypes = [I32, I32, I32, I32, I32, P, P, P, P, P]
+    lib.mla_tier_plan.restype = I32
+    lib.mla_row_copy.argtypes = [P, P, P, I32, I32, ctypes.c_int64, I32, P]
+    lib.mla_row_copy.restype = I32
     lib.mla_split_combine.argtypes = [SP, P, P, I32, P, SZ, F, P, P, P]
     lib.mla_split_combine.restype = I32
     lib.mla_lse_merge.argtypes = [I32, I32, P, P, P, P, P]

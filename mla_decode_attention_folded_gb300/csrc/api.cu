@@ -72,11 +72,18 @@ int32_t mla_plan_splits(const mla_shape* shape, const int32_t* seq_lens, int32_t
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
-                          const int32_t* block_table, const int32_t* seq_lens, float bmm1_scale,
-                          float bmm2_scale, const int32_t* counts, int32_t* work,
-                          int32_t list_len, void* workspace, size_t workspace_bytes_given,
-                          void* out, float* lse, int32_t* status, mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// mla_folded_decode with an explicit pipeline-wait bound and the
+// failure-detection test's withheld copy.
+int32_t decode_impl(const mla_shape* shape, const void* q, const void* kv,
+                    const int32_t* block_table, const int32_t* seq_lens, float bmm1_scale,
+                    float bmm2_scale, const int32_t* counts, int32_t* work, int32_t list_len,
+                    void* workspace, size_t workspace_bytes_given, void* out, float* lse,
+                    int32_t* status, mla_stream_t stream, unsigned long long wait_limit_ns,
+                    int withhold_first_copy) {
   int st = check_shape(shape);
   if (st != MLA_OK) return st;
   if (!q || !kv || !block_table || !seq_lens || !counts || !work || !out) return MLA_ERR_NULL;
@@ -118,8 +125,40 @@ int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
   a.num_pages = shape->num_pages;
   a.items = plan_items(*shape);
   a.slots = slots;
+  a.wait_limit_ns = wait_limit_ns;
+  a.withhold_first_copy = withhold_first_copy;
   cudaError_t e = launch_decode(*shape, a, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+constexpr unsigned long long kDecodeWaitLimitNs = 2000000000ull;   // 2 s
+
+}  // namespace
+
+extern "C" {
+
+int32_t mla_folded_decode(const mla_shape* shape, const void* q, const void* kv,
+                          const int32_t* block_table, const int32_t* seq_lens, float bmm1_scale,
+                          float bmm2_scale, const int32_t* counts, int32_t* work,
+                          int32_t list_len, void* workspace, size_t workspace_bytes_given,
+                          void* out, float* lse, int32_t* status, mla_stream_t stream) {
+  return decode_impl(shape, q, kv, block_table, seq_lens, bmm1_scale, bmm2_scale, counts, work,
+                     list_len, workspace, workspace_bytes_given, out, lse, status, stream,
+                     kDecodeWaitLimitNs, 0);
+}
+
+int32_t mla_folded_decode_wait_test(const mla_shape* shape, const void* q, const void* kv,
+                                    const int32_t* block_table, const int32_t* seq_lens,
+                                    float bmm1_scale, float bmm2_scale, const int32_t* counts,
+                                    int32_t* work, int32_t list_len, void* workspace,
+                                    size_t workspace_bytes_given, void* out, float* lse,
+                                    int32_t* status, uint64_t wait_limit_ns,
+                                    mla_stream_t stream) {
+  if (!status) return MLA_ERR_NULL;
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > kDecodeWaitLimitNs) return MLA_ERR_SHAPE;
+  return decode_impl(shape, q, kv, block_table, seq_lens, bmm1_scale, bmm2_scale, counts, work,
+                     list_len, workspace, workspace_bytes_given, out, lse, status, stream,
+                     wait_limit_ns, 1);
 }
 
 int32_t mla_split_combine(const mla_shape* shape, const int32_t* counts, const int32_t* work,

@@ -23,6 +23,8 @@ constexpr int kPageBytes = kPage * kDqk;          // 36864 bytes per page
 constexpr int kOCols = 64;                        // TMEM columns per 128-dim band of O^T
 constexpr int kSCol0 = 4 * kOCols;                // S^T buffers start after O^T
 constexpr uint32_t kTmemCols = 512;
+// Bound of every pipeline wait (the decode's default) and of the drain of a
+// CTA's own copies and MMAs when it stops early.
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 // When a row's lazy max moves (a score beyond the old max + 8, base 2), it is
 // set kMaxLead below the tile's max instead of at it: P = 2^(x - max) then
@@ -52,6 +54,7 @@ struct Ctl {
   Job job[2];
   uint32_t tmem_base;
   int abort_flag;
+  unsigned long long wait_limit_ns;   // DecodeArgs::wait_limit_ns
   float m_run[64];             // running row max (base-2 scores)
   float vec[64];               // rescale factors, then 1/l
   float lse[64];
@@ -65,7 +68,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ct
   while (true) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
-    if (tc::globaltimer_ns() - t0 > kTimeoutNs) {
+    if (tc::globaltimer_ns() - t0 > ctl->wait_limit_ns) {
       *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
       if (status) atomicOr(status, MLA_FAULT_WAIT_TIMEOUT);
       return false;
@@ -253,7 +256,10 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
       const int pages = (kbase + kPage < jb.j1) ? 2 : 1;
       const int pid0 = __shfl_sync(0xffffffffu, cur, (2 * t) & 31);
       const int pid1 = __shfl_sync(0xffffffffu, cur, (2 * t + 1) & 31);
-      if (lane == 0) {
+      // Failure-detection test only: CTA 0 issues no copy for its first tile,
+      // so the waits on it run out (bounded) and the CTA stops early.
+      const bool withhold = a.withhold_first_copy && blockIdx.x == 0 && g == 0;
+      if (lane == 0 && !withhold) {
         const int pid[2] = {pid0, pages == 2 ? pid1 : -1};
         const int nvalid = (pid[0] >= 0) + (pid[1] >= 0);
         uint8_t* stage = smem + st * kStageBytes;
@@ -268,7 +274,7 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
                           &ctl->kv_full[st], 512, row);
         }
       }
-      last_kv_parity[st] = (g >> 1) & 1;
+      last_kv_parity[st] = withhold ? -1 : (int)((g >> 1) & 1);
       // Tile t + kStages is requested only once PV(t) frees this stage; warmed
       // in L2 now, its copy then skips most of the HBM latency.
       if (PREFETCH && t + kStages < jb.ntiles) {

@@ -127,7 +127,7 @@ __device__ void rows_mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, ui
       } else {
         const unsigned long long now = tc::globaltimer_ns();
         if (t0 == 0) t0 = now;
-        const bool expired = now - t0 > kTimeoutNs;
+        const bool expired = now - t0 > ctl->wait_limit_ns;
         if (*reinterpret_cast<volatile int*>(&ctl->abort_flag) || expired) {
           *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
           if (expired && a.status) atomicOr(a.status, MLA_FAULT_WAIT_TIMEOUT);
@@ -264,10 +264,12 @@ __device__ void rows_softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* c
         tc::tmem_st8(sbuf + kh * 16 + c * 8, hi);
         tc::tmem_st8(sbuf + 32 + kh * 16 + c * 8, lo);
       }
-      if (kh == 0 && tl >= nvalid) {               // keys past the split: V rows must be 0
+      // Keys past the split: their V rows must be 0 in the two bands this
+      // CTA's PV reads.
+      if (kh == 0 && tl >= nvalid) {
         uint8_t* stage = smem + st * kStageBytes;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
           uint4* vrow = reinterpret_cast<uint4*>(stage + c * kChunkBytes + tl * 128);
 #pragma unroll
           for (int u = 0; u < 8; ++u) vrow[u] = make_uint4(0, 0, 0, 0);
@@ -317,8 +319,11 @@ __device__ void rows_softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* c
     tc::fence_before_sync();
     tc::mbar_arrive(&ctl->o_empty);
     if (mine && half == 0 && kh == 0) {
-      if (jb.direct && a.lse) a.lse[orow] = lse2;
-      else a.part_lse[orow] = lse2;
+      if (jb.direct) {
+        if (a.lse) a.lse[orow] = lse2;        // one-split rows have no partial slot
+      } else {
+        a.part_lse[orow] = lse2;
+      }
     }
     g += jb.ntiles;
     ++x;
@@ -356,6 +361,7 @@ decode_rows_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv
       tc::mbar_init(&ctl->job_empty[b], 1 + kGroup);   // the MMA thread + the softmax group
     }
     ctl->abort_flag = 0;
+    ctl->wait_limit_ns = a.wait_limit_ns;
     tc::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {

@@ -215,7 +215,7 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
       } else {
         const unsigned long long now = tc::globaltimer_ns();
         if (t0 == 0) t0 = now;
-        const bool expired = now - t0 > kTimeoutNs;
+        const bool expired = now - t0 > ctl->wait_limit_ns;
         if (*reinterpret_cast<volatile int*>(&ctl->abort_flag) || expired) {
           *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
           if (expired && a.status) atomicOr(a.status, MLA_FAULT_WAIT_TIMEOUT);
@@ -288,8 +288,13 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
             a.part_o[((long long)jb.item * a.M + m0 + i) * kDv + d] = 0.f;
         }
       if (gt < rows) {
-        if (jb.direct && a.lse) a.lse[(long long)jb.r * a.M + m0 + gt] = -INFINITY;
-        else a.part_lse[(long long)jb.item * a.M + m0 + gt] = -INFINITY;
+        // One-split rows have no partial slot: without an LSE output there is
+        // nothing to write for them.
+        if (jb.direct) {
+          if (a.lse) a.lse[(long long)jb.r * a.M + m0 + gt] = -INFINITY;
+        } else {
+          a.part_lse[(long long)jb.item * a.M + m0 + gt] = -INFINITY;
+        }
       }
       continue;
     }
@@ -466,8 +471,11 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
     tc::fence_before_sync();
     tc::mbar_arrive(&ctl->o_empty);
     if (gt < rows) {
-      if (jb.direct && a.lse) a.lse[(long long)jb.r * a.M + m0 + gt] = ctl->lse[gt];
-      else a.part_lse[(long long)jb.item * a.M + m0 + gt] = ctl->lse[gt];
+      if (jb.direct) {
+        if (a.lse) a.lse[(long long)jb.r * a.M + m0 + gt] = ctl->lse[gt];
+      } else {
+        a.part_lse[(long long)jb.item * a.M + m0 + gt] = ctl->lse[gt];
+      }
     }
     g += jb.ntiles;
     ++x;
@@ -507,6 +515,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
       tc::mbar_init(&ctl->job_empty[b], 1 + C::kGroup);   // the MMA thread + the softmax group
     }
     ctl->abort_flag = 0;
+    ctl->wait_limit_ns = a.wait_limit_ns;
     tc::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {

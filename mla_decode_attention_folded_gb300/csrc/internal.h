@@ -105,6 +105,9 @@ struct DecodeArgs {
   float bmm2;
   int R, M, max_pages, num_pages, items, slots;   // R, M: row groups, rows per group
   int groups;          // row group g reads request g / groups
+  unsigned long long wait_limit_ns;   // bound of every pipeline wait (drains keep their own)
+  int withhold_first_copy;            // failure-detection test: CTA 0 never issues its
+                                      // first KV tile's copy, so one wait must run out
 };
 
 // Launchers (return cudaError_t of the launch).

@@ -8,37 +8,42 @@
 // partials kept in a fixed array of device memory that belongs to this
 // library instead of a caller-provided workspace.
 //
-// The array is a file-scope __device__ object of kNoallocScratchBytes (64 MiB);
-// every GPU that loads the library holds it until the process exits. In host
-// code its name is only a host-side stand-in, so the device address is looked
-// up once per device with cudaGetSymbolAddress and cached. All calls on a
-// device share the array; nothing in it has to start at zero, because each
-// call writes every partial it later reads.
+// The array is a file-scope __device__ object of MLA_NOALLOC_SCRATCH_BYTES
+// (64 MiB); every GPU that loads the library's device code holds it until the
+// process exits. In host code its name is only a host-side stand-in, so the
+// device address is looked up with cudaGetSymbolAddress, with the device
+// current, on the first call per device, and cached. All calls on a device
+// share the array; nothing in it has to start at zero, because each call
+// writes every partial it later reads.
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = size_t(64) << 20;
+constexpr size_t kNoallocScratchBytes = MLA_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoallocScratchBytes == (size_t(64) << 20), "the header states 64 MiB");
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-void* g_scratch_addr[kMaxDevices] = {};
+// Device address of the array per device; two host threads making their first
+// call on one device at once both look it up and store the same value.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
-// The scratch array's device address on the current device (set up on the
+// The scratch array's device address on the current device (looked up on the
 // first call per device).
 int32_t scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MLA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return MLA_OK;
 }
 

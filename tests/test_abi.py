@@ -35,6 +35,15 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, name), name
 
 
+def test_noalloc_limit_matches_header():
+    """The allocation-free entry point's scratch size as the header defines it
+    (the library derives its array from the same macro) is the binding's."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+MLA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "MLA_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert int(m.group(1)) << int(m.group(2)) == _lib.NOALLOC_SCRATCH_BYTES
+
+
 @pytest.mark.parametrize("R,k,H,G,policy,ms", [
     (2, 4, 8, 8, pl.BALANCED, 64), (32, 4, 8, 152, pl.BALANCED, 64),
     (64, 7, 8, 152, pl.UNIFORM, 64), (16, 4, 64, 152, pl.BALANCED, 64),

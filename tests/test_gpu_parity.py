@@ -264,6 +264,52 @@ def test_out_of_range_page_sets_status_without_fault():
     assert status & mla.FAULT_PAGE_RANGE
 
 
+def test_wait_that_runs_out_stops_one_cta_and_the_plan_stays_reusable():
+    """Failure detection without a fault: CTA 0's first KV copy is withheld and
+    the pipeline waits are bounded at 20 ms, so a wait runs out. The call
+    returns with MLA_FAULT_WAIT_TIMEOUT set, and a regular decode of the same
+    plan and work list afterwards matches the oracle (the job counters were put
+    back). 32-row, 64-row and rows-as-M kernels."""
+    for lens, k, H in (((3000, 700, 64), 4, 8), ((2100, 640), 7, 8), ((1300, 90), 2, 64)):
+        b = make_batch_from_lengths(lens, k, H, seed=43, scaling="amax")
+        d = to_device(b)
+        eng = mla.FoldedMla(b.R, b.k, b.H, d["bt"].shape[1], d["kv"].shape[0], "cuda",
+                            num_ctas=_sms(), min_split_tokens=64)
+        bmm1, bmm2 = bmm_scales(b)
+        eng.plan(d["lens"])
+        out = torch.empty((b.R, b.M, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((b.R, b.M), dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        mla.folded_decode_wait_test(eng.shape, d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2,
+                                    eng.counts, eng.work, eng.workspace, out, lse, status,
+                                    20_000_000)
+        mla.split_combine(eng.shape, eng.counts, eng.work, eng.workspace, bmm2, out, lse)
+        torch.cuda.synchronize()
+        assert int(status.item()) & mla.FAULT_WAIT_TIMEOUT, (lens, k, H)
+        eng.status.zero_()
+        o, l = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2)
+        torch.cuda.synchronize()
+        assert int(eng.status.item()) == 0
+        ref_o, ref_l = oracle_full(b)
+        assert_close(o.float().reshape(b.R, b.M, 512).cpu(), l.cpu(), ref_o, ref_l,
+                     f"after a timed-out decode {lens}")
+
+
+def test_wait_test_entry_refuses_limits_out_of_range():
+    # Device inputs are NULL: a working range check answers MLA_ERR_SHAPE
+    # first; without it the call would stop at MLA_ERR_NULL, launching nothing.
+    import ctypes
+    from mla_decode_attention_folded_gb300 import _lib
+    s = mla.make_shape(2, 2, 8, 8, 16, _sms())
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib = _lib.load()
+    for limit in (0, 999_999, 3_000_000_000):
+        rc = lib.mla_folded_decode_wait_test(ctypes.byref(s), None, None, None, None, 0.1, 1.0,
+                                             None, None, mla.plan_list_len(s), None, 0, None,
+                                             None, status.data_ptr(), limit, None)
+        assert rc == -2, limit                                  # MLA_ERR_SHAPE
+
+
 def test_no_lse_route_matches_lse_route():
     """lse = NULL (the route without an LSE): the same out, bit for bit, on
     single- and multi-split requests and on the 32-row, 64-row and rows-as-M
@@ -286,6 +332,36 @@ def test_no_lse_route_matches_lse_route():
         ref_o, ref_l = oracle_full(b)
         assert_close(out2.float().reshape(b.R, b.M, 512).cpu(), lse1.cpu(), ref_o, ref_l,
                      f"no-lse {lens}")
+
+
+def test_no_lse_route_writes_nothing_outside_its_buffers():
+    """Without an LSE output, one-split rows have nowhere to put theirs: the
+    decode must not write it anywhere (a one-split plan needs no workspace at
+    all). Canary bytes around the workspace stay untouched; 32-row, 64-row and
+    rows-as-M kernels, one-split and mixed plans."""
+    for lens, k, H, max_splits in (((3000, 700, 0, 64), 4, 8, 1), ((2100, 640, 0), 7, 8, 1),
+                                   ((1300, 90, 0), 2, 64, 1), ((3000, 700, 0, 64), 4, 8, 64)):
+        b = make_batch_from_lengths(lens, k, H, seed=45, scaling="amax")
+        d = to_device(b)
+        s = mla.make_shape(b.R, b.k, b.H, d["bt"].shape[1], d["kv"].shape[0], _sms(), 64,
+                           max_splits, pl.UNIFORM if max_splits == 1 else pl.BALANCED)
+        ws = mla.workspace_bytes(s)
+        canary = torch.full(((ws + 255) // 256 * 256 + (1 << 20),), 0x5A, dtype=torch.uint8,
+                            device="cuda")
+        workspace = canary[:max(ws, 256)]          # never NULL: a stray write lands here
+        counts = torch.zeros(b.R, dtype=torch.int32, device="cuda")
+        work = torch.full((mla.plan_list_len(s),), -1, dtype=torch.int32, device="cuda")
+        out = torch.empty((b.R, b.M, 512), dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        mla.plan_splits(s, d["lens"], counts, work)
+        mla.folded_decode(s, d["q"], d["kv"], d["bt"], d["lens"], *bmm_scales(b), counts, work,
+                          workspace, out, None, status)
+        mla.split_combine(s, counts, work, workspace, bmm_scales(b)[1], out, None)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert bool((canary[ws:] == 0x5A).all()), (lens, k, H, max_splits)
+        ref_o, ref_l = oracle_full(b)
+        assert_close(out.float().cpu(), ref_l, ref_o, ref_l, f"no-lse {lens} {max_splits}")
 
 
 def test_lse_merge_without_lse_output():

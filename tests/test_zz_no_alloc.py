@@ -1,20 +1,22 @@
 """The allocation-free decode entry point against the regular one.
 
 mla_folded_decode_noalloc serves callers that may not allocate device memory
-(for example a host application whose own allocator owns the GPU): it keeps
-the split-KV partials in a fixed device array inside the library rather than
-in a caller workspace. This file runs last so that a failure here never hides
-the other tests; it also passes alone in a fresh process.
+(for example a host application whose own allocator owns the GPU, or code that
+runs while a memory pool is being sized): it keeps the split-KV partials in a
+fixed device array inside the library rather than in a caller workspace. On
+the same plan it runs the same kernels as mla_folded_decode followed by
+mla_split_combine, so its results must be bit-identical to theirs. This file
+runs last so that a failure here never hides the other tests; it also passes
+alone in a fresh process.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import mla_decode_attention_folded_gb300 as mla
 from mla_decode_attention_folded_gb300 import _lib
-from tests.gpu_util import assert_close, bmm_scales, to_device
+from tests.gpu_util import assert_close, bmm_scales, oracle_full, to_device
 from workloads import make_batch_from_lengths
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +39,7 @@ def _decode_both(b):
     torch.cuda.synchronize()
     assert int(status.item()) == 0 and int(eng.status.item()) == 0
     assert int(eng.counts.max()) >= 2          # the scratch really held partials
-    return (ref_o.float().cpu(), ref_l.cpu()), (out.float().cpu(), lse.cpu())
+    return (ref_o.cpu(), ref_l.cpu()), (out.cpu(), lse.cpu())
 
 
 def test_noalloc_matches_regular_entry_point_twice_in_a_row():
@@ -45,15 +47,19 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row():
     second = make_batch_from_lengths((5000, 130, 2600), 7, 8, seed=202, scaling="amax")
     for b in (first, second):
         (ro, rl), (o, l) = _decode_both(b)
-        assert_close(o.numpy(), l.numpy(), ro.numpy().astype(np.float64),
-                     rl.numpy().astype(np.float64), "no-alloc vs regular")
+        assert torch.equal(o.view(torch.int16), ro.view(torch.int16)), "out differs"
+        assert torch.equal(l, rl), "lse differs"
+        ref_o, ref_l = oracle_full(b)
+        assert_close(o.float().numpy(), l.numpy(), ref_o, ref_l, "no-alloc vs oracle")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
+    # Every device pointer is NULL: a working size check returns
+    # MLA_ERR_SCRATCH_LIMIT first; were it missing, the null checks of the
+    # decode would refuse the call before any launch.
     lib = _lib.load()
     s = mla.make_shape(1024, 64, 64, 4096, 1 << 20, 2048)      # M = 4096 rows per request
     assert mla.workspace_bytes(s) > _lib.NOALLOC_SCRATCH_BYTES
-    fake = ctypes.c_void_p(1 << 20)
-    rc = lib.mla_folded_decode_noalloc(ctypes.byref(s), fake, fake, fake, fake, 1.0, 1.0, fake,
-                                       fake, mla.plan_list_len(s), fake, fake, None, None)
+    rc = lib.mla_folded_decode_noalloc(ctypes.byref(s), None, None, None, None, 1.0, 1.0, None, None,
+                                       mla.plan_list_len(s), None, None, None, None)
     assert rc == -8                                             # MLA_ERR_SCRATCH_LIMIT
