@@ -6,7 +6,10 @@
 
 A step is one pass of the whole decode path over one synthetic batch with the
 inputs resident in HBM: the device planner, the split-KV decode and the LSE
-reduction (the fold itself is a free view). L2 is flushed before every step by
+reduction (the fold itself is a free view). The headline line is measured on
+the largest single-GPU workload (R128_k7_H64_skewed128k: 128 requests x 7
+draft tokens x 64 heads, skewed lengths); the four other workloads are
+measured the same way and reported beside it under "per_workload". L2 is flushed before every step by
 writing a buffer of twice its size; the flush is outside the timed region.
 Every step is timed with CUDA events on the launching stream. Under torchrun
 each rank decodes its own batch of the same shape (requests are independent:
@@ -37,7 +40,9 @@ from workloads import D_QK, WORKLOADS, make_batch  # noqa: E402
 
 METRIC = "decode rows/s and KV HBM GB/s (fraction of 8 TB/s) vs unfolded, 1 GB300"
 UNIT = "rows/s"
-DEFAULT_WORKLOAD = "R32_k4_H8_len1k-8k"
+DEFAULT_WORKLOAD = "R128_k7_H64_skewed128k"
+# Oracle timed single-threaded on these workloads as well (the small ones).
+ONE_THREAD_WORKLOADS = ("R2_k4_H8_len100+37", "R32_k4_H8_len1k-8k", "R64_k7_H8_lognormal2k")
 REFERENCE_BUDGET_S = 120.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -55,8 +60,11 @@ def parse():
     p.add_argument("--variant-steps", type=int, default=300)
     p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--per-workload-steps", type=int, default=200)
+    p.add_argument("--one-thread-seconds", type=float, default=3.0)
     p.add_argument("--no-variants", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-workload", action="store_true")
     return p.parse_args()
 
 
@@ -116,6 +124,25 @@ def cpu_threads() -> int:
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def one_thread_oracle(workload: str, seconds: float):
+    """The oracle's rate on one host thread: a fresh interpreter with the BLAS
+    thread count pinned to 1 before numpy loads runs the same sampler."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from workloads import make_batch; "
+            "r = bench.OracleSampler(make_batch(%r)).run(%r); "
+            "print(json.dumps(r))") % (ROOT, workload, float(seconds))
+    try:
+        p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=120 + 4 * seconds)
+        rps, rows, el, chunks = json.loads(p.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError) as e:
+        return {"workload": workload, "error": str(e)[:200]}
+    return {"workload": workload, "value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{chunks} consecutive {OracleSampler.CHUNK}-key chunks = {rows:.2f} "
+                      f"query-token rows in {el:.1f} s"}
 
 
 # ---------------------------------------------------------------- clocks
@@ -414,6 +441,37 @@ class Runner:
                 self._time(g_no_comb, steps, flush))
 
 
+class TieredRunner(Runner):
+    """The pages' tiered launch (unsplit launch + split tiers on prioritised
+    streams, built from the same kernels), timed like a Runner step."""
+
+    def __init__(self, batch, dev):
+        import mla_decode_attention_folded_gb300 as mla
+        self.mla = mla
+        self.b = batch
+        self.q = batch.q.to(dev)
+        self.kv = batch.kv.to(dev)
+        self.bt = batch.block_table.to(dev)
+        self.lens = batch.seq_lens.to(dev)
+        self.tiered = mla.TieredMla(batch.R, batch.k, batch.H, self.bt.shape[1],
+                                    self.kv.shape[0], dev)
+        self.out = torch.empty((batch.R, batch.M, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((batch.R, batch.M), dtype=torch.float32, device=dev)
+        self.bmm1 = float(np.float32(batch.sm_scale) * np.float32(batch.q_scale)
+                          * np.float32(batch.kv_scale))
+        self.bmm2 = float(batch.kv_scale)
+
+    def step(self):
+        self.tiered.decode(self.q, self.kv, self.bt, self.lens, self.bmm1, self.bmm2,
+                           out=self.out, lse=self.lse)
+
+
+def has_tiers(batch, dev) -> bool:
+    import mla_decode_attention_folded_gb300 as mla
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return len(mla.balanced_tiers(batch.R, sms)) > 0
+
+
 class L2Flush:
     """Evicts L2 before a timed step: write a buffer of twice the L2 size, then
     read another one, so L2 holds neither the inputs nor dirty lines whose
@@ -476,6 +534,64 @@ def e2e_rows_per_s(batch, dev, steps):
     return R * batch.k / (ms / 1e3), h2d, d2h
 
 
+VARIANTS = (("folded_uniform", 1, True), ("unfolded_balanced", 0, False),
+            ("unfolded_uniform", 1, False))
+
+
+def workload_summary(name, batch, step_ms, dec_ms, variants):
+    """Step time, decode time, the binding roofline and the variants of one
+    workload, with the fold and balance gains derived from them."""
+    lens = batch.seq_lens.numpy()
+    rows = batch.R * batch.k
+    kv_b = D_QK * int(lens.sum())
+    roof = roofline(algorithmic_bytes(lens, batch.M), algorithmic_flops(lens, batch.M),
+                    dec_ms / 1e3)
+    r = {"step_us": step_ms * 1e3, "decode_us": dec_ms * 1e3,
+         "rows_per_s": rows / (step_ms / 1e3),
+         "head_rows_per_s": batch.R * batch.M / (step_ms / 1e3),
+         "kv_gbs_step": kv_b / (step_ms / 1e3) / 1e9,
+         "bound": roof["bound"], "frac": roof["frac"], "hbm_frac": roof["hbm_frac"],
+         "tensor_frac": roof["tensor_frac"], "traffic": profiled_traffic(name),
+         "variants_step_us": {"folded_balanced": step_ms * 1e3}}
+    for v, ms in variants.items():
+        r["variants_step_us"][v] = ms * 1e3
+    if "folded_uniform" in variants:
+        r["balanced_over_uniform"] = variants["folded_uniform"] / step_ms
+    if "unfolded_balanced" in variants:
+        r["folded_over_unfolded"] = variants["unfolded_balanced"] / step_ms
+    if "tiered" in variants:
+        r["persistent_over_tiered"] = variants["tiered"] / step_ms
+    return r
+
+
+def measure_variants(batch, dev, flush, steps):
+    out = {}
+    for name, policy, folded in VARIANTS:
+        r = Runner(batch, dev, policy=policy, folded=folded)
+        out[name] = r.timed(steps, 5, flush)
+        del r
+    if has_tiers(batch, dev):
+        r = TieredRunner(batch, dev)
+        out["tiered"] = r.timed(steps, 5, flush)
+        del r
+    return out
+
+
+def measure_side_workload(name, dev, flush, steps, with_variants):
+    """One of the other workloads: the chained step and the decode alone, plus
+    the three variants."""
+    batch = make_batch(name)
+    r = Runner(batch, dev, policy=0, folded=True)
+    step_ms = r.timed(steps, 5, flush)
+    _, dec_ms, _ = r.kernel_times(steps, flush)
+    status = int(r.eng.status.item())
+    del r
+    variants = measure_variants(batch, dev, flush, steps) if with_variants else {}
+    out = workload_summary(name, batch, step_ms, dec_ms, variants)
+    out["status"] = status
+    return out
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
@@ -488,7 +604,6 @@ def run_ours(args):
         def barrier():
             dist.barrier()
 
-    w = WORKLOADS[args.workload]
     batch = make_batch(args.workload)
     flush = L2Flush(dev)
 
@@ -497,10 +612,11 @@ def run_ours(args):
     clocks.start()
     step_ms = main.timed(args.steps, max(args.warmup, 3), flush, barrier)
     clk = clocks.stop()
-    plan_ms, dec_ms, comb_ms = main.kernel_times(min(args.steps, 1000), flush)
+    aux_steps = min(args.steps, 1000)
+    plan_ms, dec_ms, comb_ms = main.kernel_times(aux_steps, flush)
     main.uv_setup(dev)
-    uv_step_ms, uv_ms = main.uv_times(min(args.steps, 1000), flush)
-    no_plan_ms, no_comb_ms = main.marginal_times(min(args.steps, 1000), flush)
+    uv_step_ms, uv_ms = main.uv_times(aux_steps, flush)
+    no_plan_ms, no_comb_ms = main.marginal_times(aux_steps, flush)
     status = int(main.eng.status.item())
     step_ms, dec_ms = max_over_ranks([step_ms, dec_ms], dev)
 
@@ -520,15 +636,20 @@ def run_ours(args):
         in_chain = {"decode_ms": dec_chain_ms, "achieved": rc["achieved"], "frac": rc["frac"],
                     "unit": rc["unit"]}
 
-    variants = {}
+    variants_ms = {}
     if rank == 0 and not args.no_variants:
-        for name, policy, folded in (("folded_uniform", 1, True), ("unfolded_balanced", 0, False),
-                                     ("unfolded_uniform", 1, False)):
-            r = Runner(batch, dev, policy=policy, folded=folded)
-            ms = r.timed(args.variant_steps, 5, flush)
-            variants[name] = {"rows_per_s": rows / (ms / 1e3), "ms_per_step": ms,
-                              "kv_gbs": kv_b / (ms / 1e3) / 1e9}
-            del r
+        variants_ms = measure_variants(batch, dev, flush, args.variant_steps)
+    variants = {name: {"rows_per_s": rows / (ms / 1e3), "ms_per_step": ms,
+                       "kv_gbs": kv_b / (ms / 1e3) / 1e9} for name, ms in variants_ms.items()}
+
+    per_workload = {}
+    if rank == 0 and not args.no_per_workload:
+        per_workload[args.workload] = workload_summary(args.workload, batch, step_ms, dec_ms,
+                                                       variants_ms)
+        for name in WORKLOADS:
+            if name != args.workload:
+                per_workload[name] = measure_side_workload(
+                    name, dev, flush, args.per_workload_steps, not args.no_variants)
 
     e2e_v, h2d, d2h = e2e_rows_per_s(batch, dev, args.e2e_steps)
     if world > 1:
@@ -543,7 +664,9 @@ def run_ours(args):
         cpu = {"value": rps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                "sample": f"{chunks} consecutive {OracleSampler.CHUNK}-key chunks of the "
                          f"requests of {args.workload} = {cpu_rows:.1f} query-token rows (the batch "
-                         f"has {batch.R * batch.k}; {el:.1f} s, float64 numpy)"}
+                         f"has {batch.R * batch.k}; {el:.1f} s, float64 numpy)",
+               "one_thread": [one_thread_oracle(w, args.one_thread_seconds)
+                              for w in ONE_THREAD_WORKLOADS]}
 
     if rank != 0:
         return
@@ -555,7 +678,8 @@ def run_ours(args):
         "config": {"workload": args.workload, "R": batch.R, "k": batch.k, "H": batch.H,
                    "M": batch.M, "policy": "balanced", "num_ctas": main.eng.shape.num_ctas,
                    "kv_tokens": int(lens.sum()), "accumulate": "f32",
-                   "l2": "flushed before every step (2x L2 write + 2x L2 read, untimed)", "timing": "CUDA graph per step, events around each replay",
+                   "l2": "flushed before every step (2x L2 write + 2x L2 read, untimed)",
+                   "timing": "CUDA graph per step, events around each replay",
                    "parallelism": f"replicas{world}"},
         "kv_gbs": kv_b / (step_ms / 1e3) / 1e9,
         "kv_frac_of_8tbs": kv_b / (step_ms / 1e3) / 8e12,
@@ -563,6 +687,7 @@ def run_ours(args):
         "kernel_ms": {"plan": plan_ms, "decode": dec_ms, "combine": comb_ms},
         "chain_ms": {"step": step_ms, "without_plan": no_plan_ms, "without_combine": no_comb_ms},
         "variants": variants,
+        "per_workload": per_workload,
         "w_uv": {"step_ms": uv_step_ms, "rows_per_s": world * rows / (uv_step_ms / 1e3),
                  "uv_kernel_ms": uv_ms,
                  "what": "plan -> decode (no LSE) -> split reduction fused with the W_UV "

@@ -56,3 +56,21 @@ def test_source_hash_ignores_comments_only():
     assert bench.strip_comments(code) == bench.strip_comments(commented)
     assert bench.strip_comments(code) != bench.strip_comments(changed)
     assert len(bench.source_hash()) == 16
+
+
+def test_one_thread_oracle_runs_in_its_own_interpreter():
+    r = bench.one_thread_oracle("R2_k4_H8_len100+37", 0.2)
+    assert "error" not in r, r
+    assert r["cores"] == 1 and r["kind"] == "oracle" and r["value"] > 0
+
+
+def test_workload_summary_gains():
+    b = make_batch_from_lengths([640, 64], 2, 4, seed=7)
+    s = bench.workload_summary("none", b, 0.02, 0.015,
+                               {"folded_uniform": 0.03, "unfolded_balanced": 0.05})
+    assert s["step_us"] == pytest.approx(20.0) and s["decode_us"] == pytest.approx(15.0)
+    assert s["balanced_over_uniform"] == pytest.approx(1.5)
+    assert s["folded_over_unfolded"] == pytest.approx(2.5)
+    assert s["rows_per_s"] == pytest.approx(b.R * b.k / 0.02e-3)
+    assert s["traffic"] is None            # no capture of a workload called "none"
+    assert s["variants_step_us"]["folded_balanced"] == pytest.approx(20.0)
