@@ -158,8 +158,10 @@ int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t
  * exceeds it by at most 8 (2^8, balanced-MLA page, module overview) and, when
  * it moves, is set 2 below the new maximum (P's small values then stay in
  * E4M3's normal range); P is fed
- * to the PV product as FP8 E4M3, unscaled, as the sum of two E4M3 terms
- * (hi = e4m3(p), lo = e4m3(p - hi)); the normaliser is the FP32 sum of p. */
+ * to the PV product as FP8 E4M3, unscaled, as the sum of two E4M3 terms built
+ * from p rounded to FP16 (p16 = fp16(p), hi = e4m3(p16), lo = e4m3(p16 - hi),
+ * each rounding to nearest even: hi + lo is p to about 2^-8 relative, the
+ * FP16 step adding at most 2^-11); the normaliser is the FP32 sum of p. */
 int32_t mla_folded_decode(const mla_shape *shape, const void *q, const void *kv,
                           const int32_t *block_table, const int32_t *seq_lens,
                           float bmm1_scale, float bmm2_scale, const int32_t *counts,

@@ -309,6 +309,13 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
 }
 
 // ---------------------------------------------------------------- P conversion
+// P (FP32, <= 2^8) enters the PV product as two E4M3 terms built in FP16:
+// p16 = fp16(p) (round to nearest even, relative error <= 2^-11),
+// hi = e4m3(p16), lo = e4m3(p16 - hi), all conversions round to nearest even
+// with satfinite; p16 - hi is exact in FP16 (hi is p16 rounded to 4
+// significant bits, so both lie within a factor of two). hi + lo is p to
+// about 2^-8 relative; the FP16 step adds at most 2^-11. FP16 pairs keep the
+// conversion at a few instructions per two values.
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -27,8 +27,8 @@
 // * Softmax in base 2 with a lazily updated row max: the max moves only when a
 //   new score exceeds it by more than 8 (P <= 2^8, balanced-MLA page, module
 //   overview), and then to 2 below the tile's max (kMaxLead). P enters the PV
-//   MMA as FP8 E4M3, unscaled, split into two E4M3 terms hi = e4m3(p),
-//   lo = e4m3(p - hi) (both FP8 operands: one E4M3 term alone misses the
+//   MMA as FP8 E4M3, unscaled, split into two E4M3 terms hi = e4m3(p16),
+//   lo = e4m3(p16 - hi), p16 = fp16(p) (both FP8 operands: one E4M3 term alone misses the
 //   +-(2e-2 + 2e-2|ref|) bound on short requests). The normaliser is the FP32
 //   sum of p.
 // * Every mbarrier wait is bounded (2 s); on expiry the CTA sets
@@ -370,9 +370,9 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
           tc::tmem_wait_st();
         }
       }
-      // P buffer st is free once PV(gg - 2) finished.
-      if (gg >= 2 && !(ok = wait_bar(&ctl->pv_done[st], ((gg >> 1) - 1) & 1, ctl, a.status)))
-        break;
+      // P buffer st is free: PV(gg - 2), the last reader of this buffer and of
+      // KV stage st, finished before the producer refilled that stage with
+      // tile gg, whose S this thread has just read.
       uint32_t hi[RT / 4], lo[RT / 4];
 #pragma unroll
       for (int i = 0; i < RT; i += 4) {

@@ -20,24 +20,11 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Two floats -> two E4M3 codes (round to nearest even, saturate to +-448),
-// low byte from `lo_val`.
-__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo_val, float hi_val) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi_val), "f"(lo_val));
-  return r;
-}
 // Two E4M3 codes -> two halves (exact), low byte to the low half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
-}
-__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
-  float2 f;
-  asm("{.reg .f16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;}"
-      : "=f"(f.x), "=f"(f.y) : "r"(h));
-  return f;
 }
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   uint16_t r;
