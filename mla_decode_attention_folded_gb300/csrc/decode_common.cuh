@@ -20,8 +20,6 @@ constexpr int kChunkBytes = kTileKeys * 128;      // one 128-dim latent band of 
 constexpr int kRopeBytes = kTileKeys * 64;        // the 64 rope dims of a tile
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;     // 73728
 constexpr int kPageBytes = kPage * kDqk;          // 36864 bytes per page
-constexpr int kOCols = 64;                        // TMEM columns per 128-dim band of O^T
-constexpr int kSCol0 = 4 * kOCols;                // S^T buffers start after O^T
 constexpr uint32_t kTmemCols = 512;
 // Bound of every pipeline wait (the decode's default) and of the drain of a
 // CTA's own copies and MMAs when it stops early.

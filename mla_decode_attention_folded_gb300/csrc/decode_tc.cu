@@ -43,21 +43,45 @@ using namespace dec;
 
 template <int NR>
 struct Cfg {
-  static constexpr bool kHiloN = NR == 32;        // hi|lo side by side along N
   static constexpr int kHalves = 2;               // 128-thread softmax groups per row block
   static constexpr int kRowsPerThread = NR / kHalves;
   static constexpr int kGroup = 128 * kHalves;    // softmax threads
   static constexpr int kThreads = 64 + kGroup;    // + the TMA warp and the MMA warp
   static constexpr int kQChunk = NR * 128;
   static constexpr int kQBytes = 4 * kQChunk + NR * 64;
-  static constexpr int kPBytes = kHiloN ? kTileKeys * 64 : 2 * kTileKeys * 64;
+  // P^T of a tile: one row per key holding the hi codes of the NR query rows,
+  // then their lo codes (2*NR bytes: 64-byte swizzle for NR = 32, 128-byte for
+  // NR = 64).
+  static constexpr int kPRow = 2 * NR;
+  static constexpr int kPBytes = kTileKeys * kPRow;
+  static constexpr tc::Swizzle kPSw = NR == 32 ? tc::kSw64 : tc::kSw128;
+  static constexpr int kPAtom = 8 * kPRow;        // 8-key group stride of P^T
+  // O^T in TMEM, one 128-dim value band after another. A "split" band keeps
+  // the hi and lo products in separate accumulators side by side (NR columns
+  // each) so that one MMA of N = 2*NR covers both terms; the others take the
+  // two terms as two N = NR MMAs into one accumulator. NR = 32: all four bands
+  // split (256 columns) beside two S^T buffers. NR = 64: bands 0-2 split and
+  // band 3 not (448 columns) beside one S^T buffer, which the softmax frees as
+  // soon as it has read S into registers, before the next tile's S is usually
+  // ready to issue anyway.
+  static constexpr int kSplitBands = NR == 32 ? 4 : 3;
+  static constexpr int kSBufs = NR == 32 ? 2 : 1;
+  __host__ __device__ static constexpr bool split(int dt) { return dt < kSplitBands; }
+  __host__ __device__ static constexpr int band_col(int dt) {
+    return dt < kSplitBands ? dt * 2 * NR : kSplitBands * 2 * NR + (dt - kSplitBands) * NR;
+  }
+  static constexpr int kSCol = band_col(4);       // S^T buffers after O^T
+  __host__ __device__ static constexpr int s_col(uint32_t gg) {
+    return kSCol + (int)(gg % kSBufs) * NR;
+  }
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffP = kOffQ + kQBytes;
   static constexpr int kOffCtl = kOffP + 2 * kPBytes;
   static constexpr uint32_t kIdescS = tc::idesc_e4m3_f32(128, NR, false, false);
-  static constexpr uint32_t kIdescPV = tc::idesc_e4m3_f32(128, 64, true, true);
+  static constexpr uint32_t kIdescPVSplit = tc::idesc_e4m3_f32(128, 2 * NR, true, true);
+  static constexpr uint32_t kIdescPVOne = tc::idesc_e4m3_f32(128, NR, true, true);
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1 KB alignment");
-  static_assert(kSCol0 + 2 * NR <= (int)kTmemCols, "TMEM budget");
+  static_assert(kSCol + kSBufs * NR <= (int)kTmemCols, "TMEM budget");
 };
 
 // Reduce v[32] across the 32 lanes by halving exchanges (31 shuffles per
@@ -127,7 +151,7 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
 
   auto issue_s = [&](uint32_t gg) {
     const int st = gg & 1;
-    const uint32_t d = tmem + kSCol0 + st * NR;
+    const uint32_t d = tmem + C::s_col(gg);
     const uint32_t kv = s_kv + st * kStageBytes;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -155,19 +179,18 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
         // V^T band dt, keys 32kk..32kk+31: MN-major, 8-key groups 1 KB apart.
         const uint64_t va = tc::smem_desc(kv + dt * kChunkBytes + kk * 32 * 128, kChunkBytes,
                                           1024, tc::kSw128);
+        // P^T rows of these 32 keys: the hi codes, then the lo codes, of NR rows.
+        const uint32_t pk = p + kk * 32 * C::kPRow;
         const bool acc = !(first && kk == 0);
-        if constexpr (C::kHiloN) {
-          tc::mma_e4m3(tmem + dt * kOCols, va,
-                       tc::smem_desc(p + kk * 32 * 64, kTileKeys * 64, 512, tc::kSw64),
-                       C::kIdescPV, acc);
-        } else {
-          tc::mma_e4m3(tmem + dt * kOCols, va,
-                       tc::smem_desc(p + kk * 32 * 64, kTileKeys * 64, 512, tc::kSw64),
-                       C::kIdescPV, acc);
-          tc::mma_e4m3(tmem + dt * kOCols, va,
-                       tc::smem_desc(p + kTileKeys * 64 + kk * 32 * 64, kTileKeys * 64, 512,
-                                     tc::kSw64),
-                       C::kIdescPV, true);
+        if (C::split(dt)) {          // one N = 2*NR MMA: hi and lo accumulate apart
+          tc::mma_e4m3(tmem + C::band_col(dt), va,
+                       tc::smem_desc(pk, C::kPBytes, C::kPAtom, C::kPSw), C::kIdescPVSplit, acc);
+        } else {                     // two N = NR MMAs into one accumulator
+          tc::mma_e4m3(tmem + C::band_col(dt), va,
+                       tc::smem_desc(pk, C::kPBytes, C::kPAtom, C::kPSw), C::kIdescPVOne, acc);
+          tc::mma_e4m3(tmem + C::band_col(dt), va,
+                       tc::smem_desc(pk + NR, C::kPBytes, C::kPAtom, C::kPSw), C::kIdescPVOne,
+                       true);
         }
       }
     }
@@ -201,8 +224,12 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
       if (ns < jb.ntiles && ns <= npv + 1) {
         const uint32_t gg = g + ns;
         const int st = gg & 1;
+        // Its S^T buffer is free once the softmax read the S that used it last
+        // (tile gg - kSBufs; s_empty is indexed by tile parity).
+        const uint32_t gp = gg - C::kSBufs;
         if (tc::mbar_test_wait(&ctl->kv_full[st], (gg >> 1) & 1) &&
-            (gg < 2 || tc::mbar_test_wait(&ctl->s_empty[st], ((gg >> 1) - 1) & 1))) {
+            (gg < (uint32_t)C::kSBufs ||
+             tc::mbar_test_wait(&ctl->s_empty[gp & 1], (gp >> 1) & 1))) {
           tc::fence_after_sync();
           issue_s(gg);
           if (ns == jb.ntiles - 1) tc::mma_commit(&ctl->q_empty);   // every S of the job issued
@@ -312,7 +339,7 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
       float xv[RT];
       {
         uint32_t raw[RT];
-        tmem_ld_rows<RT>(tmem + lane_addr + kSCol0 + st * NR + r0, raw);
+        tmem_ld_rows<RT>(tmem + lane_addr + C::s_col(gg) + r0, raw);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < RT; ++i) xv[i] = __uint_as_float(raw[i]);
@@ -356,9 +383,9 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
 #pragma unroll
           for (int dt = 0; dt < 4; ++dt) {
 #pragma unroll
-            for (int h = 0; h < (C::kHiloN ? 2 : 1); ++h) {
+            for (int h = 0; h < (C::split(dt) ? 2 : 1); ++h) {
               uint32_t raw[RT];
-              const uint32_t addr = tmem + lane_addr + dt * kOCols + h * 32 + r0;
+              const uint32_t addr = tmem + lane_addr + C::band_col(dt) + h * NR + r0;
               tmem_ld_rows<RT>(addr, raw);
               tc::tmem_wait_ld();
 #pragma unroll
@@ -389,22 +416,20 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
         hi[i / 4] = (uint32_t)e01 | ((uint32_t)e23 << 16);
         lo[i / 4] = (uint32_t)l01 | ((uint32_t)l23 << 16);
       }
-      // P^T row of this key, MN-major with the 64-byte swizzle: 16-byte chunk c
-      // (16 rows) of key k lives at k*64 + ((c ^ ((k >> 1) & 3)) * 16). 32-row
-      // kernel: chunks 0-1 hold hi, 2-3 lo; 64-row kernel: hi and lo in two
-      // planes. This thread writes the chunks of its rows r0 .. r0 + RT - 1.
+      // P^T row of this key, MN-major: kPRow bytes (the hi codes of the NR query
+      // rows, then their lo codes) in 16-byte chunks of 16 rows, swizzled: with
+      // the 64-byte swizzle chunk c of key k lives at k*64 + ((c ^ ((k >> 1) & 3))
+      // * 16), with the 128-byte swizzle at k*128 + ((c ^ (k & 7)) * 16). This
+      // thread writes the chunks of its rows r0 .. r0 + RT - 1 in both halves.
       uint8_t* pbuf = smem + C::kOffP + st * C::kPBytes;
-      const int sw = (tl >> 1) & 3;
+      const int sw = NR == 32 ? (tl >> 1) & 3 : tl & 7;
       const int cb = r0 / 16;
-      uint4* rh = reinterpret_cast<uint4*>(pbuf + tl * 64);
-      uint4* rl = C::kHiloN ? rh + 2 : reinterpret_cast<uint4*>(pbuf + kTileKeys * 64 + tl * 64);
+      uint4* row = reinterpret_cast<uint4*>(pbuf + tl * C::kPRow);
 #pragma unroll
       for (int j = 0; j < RT / 16; ++j) {
-        const int ch = C::kHiloN ? (cb + j) ^ sw : (cb + j) ^ sw;
-        const int cl = C::kHiloN ? (2 + cb + j) ^ sw : (cb + j) ^ sw;
-        rh[ch] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
-        (C::kHiloN ? rh : rl)[cl] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2],
-                                                lo[4 * j + 3]);
+        row[(cb + j) ^ sw] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+        row[(NR / 16 + cb + j) ^ sw] =
+            make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
       }
       if (!valid) {                                // keys past the split: V rows must be 0
         uint8_t* stage = smem + st * kStageBytes;
@@ -442,16 +467,16 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
 #pragma unroll 1
     for (int dt = 0; dt < 4; ++dt) {
       float o[RT];
-      if constexpr (C::kHiloN) {
+      if (C::split(dt)) {                          // hi and lo accumulators side by side
         uint32_t rh[RT], rl[RT];
-        tmem_ld_rows<RT>(tmem + lane_addr + dt * kOCols + r0, rh);
-        tmem_ld_rows<RT>(tmem + lane_addr + dt * kOCols + 32 + r0, rl);
+        tmem_ld_rows<RT>(tmem + lane_addr + C::band_col(dt) + r0, rh);
+        tmem_ld_rows<RT>(tmem + lane_addr + C::band_col(dt) + NR + r0, rl);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < RT; ++i) o[i] = __uint_as_float(rh[i]) + __uint_as_float(rl[i]);
       } else {
         uint32_t raw[RT];
-        tmem_ld_rows<RT>(tmem + lane_addr + dt * kOCols + r0, raw);
+        tmem_ld_rows<RT>(tmem + lane_addr + C::band_col(dt) + r0, raw);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < RT; ++i) o[i] = __uint_as_float(raw[i]);
