@@ -46,8 +46,7 @@ ONE_THREAD_WORKLOADS = ("R2_k4_H8_len100+37", "R32_k4_H8_len1k-8k", "R64_k7_H8_l
 REFERENCE_BUDGET_S = 120.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-DECODE_SOURCES = ("decode_tc.cu", "decode_rows.cu", "decode_common.cuh", "internal.h", "ptx.cuh",
-                  "tc.cuh")
+DECODE_SOURCES = ("decode_tc.cu", "decode_common.cuh", "internal.h", "ptx.cuh", "tc.cuh")
 
 
 def parse():

@@ -1,7 +1,7 @@
-// Pieces shared by the two split-KV decode kernels (decode_tc.cu: query rows
-// as the MMA's N; decode_rows.cu: query rows as the MMA's M): tile geometry,
-// the control block with its mbarriers, bounded waits, per-job facts, the TMA
-// producer warp and tensor-map encoding.
+// Pieces of the split-KV decode kernel (decode_tc.cu) kept apart from its MMA
+// and softmax roles: tile geometry, the control block with its mbarriers,
+// bounded waits, per-job facts, job claiming, the TMA producer warp, the P
+// conversion helpers and tensor-map encoding.
 #pragma once
 
 #include <cuda.h>
@@ -169,12 +169,11 @@ __device__ __forceinline__ void finish_jobs(const DecodeArgs& a) {
 // Runs on all 32 lanes of warp 0: the lanes fetch the job's block-table
 // entries 32 at a time (lane i holds page i of the chunk, checked against the
 // cache), lane 0 waits on the ring and issues the TMA copies.
-// QROWS: query rows per Q block; SHARE: consecutive jobs of an item that
-// use the same Q block; OFFQ: shared-memory offset of the Q block; STAGGER:
-// request the CTA's second tile only once its first has landed; PREFETCH:
-// with each tile, warm L2 with the pages of the tile that will next use the
-// same stage.
-template <int QROWS, int SHARE, int OFFQ, bool STAGGER, bool PREFETCH>
+// QROWS: query rows per Q block (the job's row block); OFFQ: shared-memory
+// offset of the Q block; STAGGER: request the CTA's second tile only once its
+// first has landed; PREFETCH: with each tile, warm L2 with the pages of the
+// tile that will next use the same stage.
+template <int QROWS, int OFFQ, bool STAGGER, bool PREFETCH>
 __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
                          const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
                          const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
@@ -231,7 +230,7 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
     if (x > 0 && !(ok = wait0(&ctl->q_empty, (x - 1) & 1))) break;
     if (lane == 0) {
       uint8_t* q = smem + OFFQ;
-      const int qrow = (blk / SHARE) * QROWS;
+      const int qrow = blk * QROWS;
       tc::mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
       for (int c = 0; c < 4; ++c)
         tc::tma_load_3d(q + c * kQChunk, tm_q, &ctl->q_full, c * 128, qrow, jb.r);

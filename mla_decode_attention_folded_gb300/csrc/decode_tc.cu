@@ -571,7 +571,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
   grid_dep_wait();      // the plan is complete; earlier readers of out/workspace are done
   grid_dep_launch();    // the reducer may launch; it still waits for this grid to finish
   if (warp == 0) {
-    producer<NR, 1, Cfg<NR>::kOffQ, NR == 32, NR != 32>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
+    producer<NR, Cfg<NR>::kOffQ, NR == 32, NR != 32>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer<NR>(a, smem, ctl, tmem, nb);
   } else {
@@ -622,7 +622,6 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
 }  // namespace
 
 cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
-  if (rows_as_m(a.M)) return launch_decode_rows(s, a, st);   // query rows as the MMA's M
   return row_block(a.M) == 32 ? launch_nr<32>(s, a, st) : launch_nr<64>(s, a, st);
 }
 

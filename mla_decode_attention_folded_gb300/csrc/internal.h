@@ -20,21 +20,11 @@ constexpr int kMaxM = 4096;
 
 __host__ __device__ inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// Jobs per work item. Query rows as the MMA's N (decode_tc.cu): blocks of 32
-// rows (M <= 32) or 64 rows. Query rows as the MMA's M (decode_rows.cu), used
-// from 128 rows on when 128-row blocks pad at most 1/16 of the rows: blocks of
-// 128 rows, each split into two jobs by half of the 512 output dims.
-__host__ __device__ inline bool rows_as_m(int M) {
-  const int padded = (M + 127) / 128 * 128;
-  return M >= 128 && (padded - M) * 16 <= padded;
-}
-__host__ __device__ inline int row_block(int M) {
-  return rows_as_m(M) ? 128 : (M <= 32 ? 32 : 64);
-}
-__host__ __device__ inline int row_blocks(int M) {
-  const int b = (M + row_block(M) - 1) / row_block(M);
-  return rows_as_m(M) ? 2 * b : b;
-}
+// Jobs per work item: blocks of the request's M query rows, processed with the
+// query rows as the MMA's N dimension (decode_tc.cu): blocks of 32 rows when
+// M <= 32, else of 64 rows.
+__host__ __device__ inline int row_block(int M) { return M <= 32 ? 32 : 64; }
+__host__ __device__ inline int row_blocks(int M) { return (M + row_block(M) - 1) / row_block(M); }
 // Concurrent work items the plan targets.
 __host__ __device__ inline int plan_units(int M, int num_ctas) {
   int u = num_ctas / row_blocks(M);
@@ -117,7 +107,6 @@ cudaError_t launch_combine(const mla_shape& s, const int32_t* counts, const int3
                            int list_len, const float* part_o, const float* part_lse, int slots,
                            float bmm2, uint16_t* out, float* lse, cudaStream_t st);
 cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st);
-cudaError_t launch_decode_rows(const mla_shape& s, const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_uv(const mla_shape& s, const int32_t* counts, const int32_t* work,
                       int list_len, const float* part_o, const float* part_lse, int slots,
                       float bmm2, const uint16_t* out, const uint16_t* w_uv, uint16_t* y,

@@ -14,10 +14,8 @@ formula; the one below is this project's reading:
 
 * pages p_i = ceil(len_i / 64); T = sum p_i; Rn = number of non-empty requests.
 * A request's M = k*H query rows are processed in row blocks of NR rows
-  (NR = 32 when M <= 32, else 64; NR = 128 when M >= 128 and 128-row blocks
-  pad at most 1/16 of the rows, each block then split into two jobs by
-  output-dim half), nb jobs per item. The plan targets
-  U = max(1, num_ctas // nb) concurrent work items.
+  (NR = 32 when M <= 32, else 64), nb = ceil(M / NR) jobs per item. The plan
+  targets U = max(1, num_ctas // nb) concurrent work items.
 * balanced: c0 = max(minp, ceil(T / U)) pages per split, minp =
   ceil(min_split_tokens / 64). If every non-empty request fits in one wave
   (Rn <= U) the chunk c is the smallest c >= c0 whose item count
@@ -48,25 +46,13 @@ def cdiv(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def rows_as_m(M: int) -> bool:
-    """Whether a request's rows run as 128-row blocks split by output-dim half
-    (from 128 rows on, when the blocks pad at most 1/16 of the rows)."""
-    padded = cdiv(M, 128) * 128
-    return M >= 128 and (padded - M) * 16 <= padded
-
-
 def row_block(M: int) -> int:
-    if rows_as_m(M):
-        return 128
     return 32 if M <= 32 else 64
 
 
 def row_blocks(M: int) -> int:
-    """Jobs a work item is processed as: blocks of the request's M query rows,
-    each block twice (one job per half of the 512 output dims) when the rows
-    run as 128-row blocks."""
-    b = cdiv(M, row_block(M))
-    return 2 * b if rows_as_m(M) else b
+    """Jobs a work item is processed as: blocks of the request's M query rows."""
+    return cdiv(M, row_block(M))
 
 
 def units(M: int, num_ctas: int) -> int:

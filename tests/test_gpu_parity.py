@@ -190,8 +190,8 @@ def test_maximum_row_groups():
 
 
 def test_maximum_rows_per_request():
-    """M = k * H = 4096 query rows per request (the largest M): the rows-as-M
-    kernel with 32 row blocks of 128 rows."""
+    """M = k * H = 4096 query rows per request (the largest M): 64 row blocks
+    of 64 rows per work item."""
     b = make_batch_from_lengths((700, 130), 16, 256, seed=29, scaling="amax")
     ref_o, ref_l = oracle_full(b)
     out, lse, status, _ = run_decode(b, min_split_tokens=64)
@@ -221,7 +221,7 @@ def test_many_splits_of_one_request():
 @pytest.mark.parametrize("lens,k,H,G,groups,policy", [
     ((6000,) + (300,) * 30 + (0, 90), 4, 8, 5, 1, pl.BALANCED),   # 32-row kernel, an empty request
     ((4000, 2500) + (700,) * 12, 7, 8, 7, 1, pl.BALANCED),       # 64-row kernel
-    ((3000, 1500, 400, 64), 2, 64, 3, 1, pl.BALANCED),           # rows-as-M kernel
+    ((3000, 1500, 400, 64), 2, 64, 3, 1, pl.BALANCED),           # M = 128: two 64-row blocks
     ((5000, 900, 60) + (400,) * 9, 4, 16, 6, 2, pl.BALANCED),    # row groups, 32-row blocks
     ((2500, 1800, 0, 700), 2, 64, 4, 2, pl.BALANCED),            # row groups, 64-row blocks
     ((3000, 100) + (500,) * 6, 4, 8, 3, 1, pl.UNIFORM),          # uniform splits
@@ -269,7 +269,7 @@ def test_wait_that_runs_out_stops_one_cta_and_the_plan_stays_reusable():
     the pipeline waits are bounded at 20 ms, so a wait runs out. The call
     returns with MLA_FAULT_WAIT_TIMEOUT set, and a regular decode of the same
     plan and work list afterwards matches the oracle (the job counters were put
-    back). 32-row, 64-row and rows-as-M kernels."""
+    back). 32-row kernel, 64-row kernel with one and with two row blocks."""
     for lens, k, H in (((3000, 700, 64), 4, 8), ((2100, 640), 7, 8), ((1300, 90), 2, 64)):
         b = make_batch_from_lengths(lens, k, H, seed=43, scaling="amax")
         d = to_device(b)
@@ -312,8 +312,8 @@ def test_wait_test_entry_refuses_limits_out_of_range():
 
 def test_no_lse_route_matches_lse_route():
     """lse = NULL (the route without an LSE): the same out, bit for bit, on
-    single- and multi-split requests and on the 32-row, 64-row and rows-as-M
-    kernels."""
+    single- and multi-split requests and on the 32-row and 64-row kernels, with
+    one and two 64-row blocks."""
     for lens, k, H in (((3000, 700, 64, 0), 4, 8), ((2100, 640), 7, 8), ((1300, 90), 2, 64)):
         b = make_batch_from_lengths(lens, k, H, seed=41, scaling="amax")
         d = to_device(b)
@@ -338,7 +338,7 @@ def test_no_lse_route_writes_nothing_outside_its_buffers():
     """Without an LSE output, one-split rows have nowhere to put theirs: the
     decode must not write it anywhere (a one-split plan needs no workspace at
     all). Canary bytes around the workspace stay untouched; 32-row, 64-row and
-    rows-as-M kernels, one-split and mixed plans."""
+    one and two 64-row blocks, one-split and mixed plans."""
     for lens, k, H, max_splits in (((3000, 700, 0, 64), 4, 8, 1), ((2100, 640, 0), 7, 8, 1),
                                    ((1300, 90, 0), 2, 64, 1), ((3000, 700, 0, 64), 4, 8, 64)):
         b = make_batch_from_lengths(lens, k, H, seed=45, scaling="amax")

@@ -61,7 +61,7 @@ def _decode_uv(b, w_dev, groups=1, policy=mla.POLICY_BALANCED, min_split_tokens=
 @pytest.mark.parametrize("lens,k,H,groups", [
     ((3000, 700, 64, 0), 4, 8, 1),        # multi-split, single-split and an empty request
     ((2100, 640, 90), 7, 8, 1),           # 21 tokens: one ragged 32-token block
-    ((1300, 90), 4, 64, 1),               # rows-as-M decode; 64 heads
+    ((1300, 90), 4, 64, 1),               # M = 256: four 64-row blocks; 64 heads
     ((1300, 900), 4, 64, 2),              # row groups (the pages' partial fold)
     ((500,) * 9, 4, 2, 1),                # 36 tokens: two blocks, the second ragged
 ])
