@@ -57,6 +57,7 @@ struct Ctl {
   float vec[64];               // rescale factors, then 1/l
   float lse[64];
   float red[4][64];            // cross-warp reduction scratch
+  uint64_t pv_half[kStages];   // MMA -> TMA: PV is done with value bands 0-1 (HALVES)
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ctl,
@@ -172,8 +173,9 @@ __device__ __forceinline__ void finish_jobs(const DecodeArgs& a) {
 // QROWS: query rows per Q block (the job's row block); OFFQ: shared-memory
 // offset of the Q block; STAGGER: request the CTA's second tile only once its
 // first has landed; PREFETCH: with each tile, warm L2 with the pages of the
-// tile that will next use the same stage.
-template <int QROWS, int OFFQ, bool STAGGER, bool PREFETCH>
+// tile that will next use the same stage; HALVES: refill a stage in two
+// halves (below).
+template <int QROWS, int OFFQ, bool STAGGER, bool PREFETCH, bool HALVES>
 __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
                          const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
                          const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
@@ -243,7 +245,8 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
         nxt = fetch(jb, (t >> 4) + 1);
       }
       const int st = g & 1;
-      if (g >= 2 && !(ok = wait0(&ctl->pv_done[st], ((g >> 1) - 1) & 1))) break;
+      if constexpr (!HALVES)
+        if (g >= 2 && !(ok = wait0(&ctl->pv_done[st], ((g >> 1) - 1) & 1))) break;
       // Every CTA starts at once. With short, HBM-bound jobs it pays to ask
       // for the second tile only after the first has landed: the first tiles
       // then arrive first and the MMAs start while the second ones stream in,
@@ -256,22 +259,56 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
       // Failure-detection test only: CTA 0 issues no copy for its first tile,
       // so the waits on it run out (bounded) and the CTA stops early.
       const bool withhold = a.withhold_first_copy && blockIdx.x == 0 && g == 0;
-      if (lane == 0 && !withhold) {
-        const int pid[2] = {pid0, pages == 2 ? pid1 : -1};
-        const int nvalid = (pid[0] >= 0) + (pid[1] >= 0);
-        uint8_t* stage = smem + st * kStageBytes;
-        tc::mbar_arrive_expect_tx(&ctl->kv_full[st], nvalid * kPageBytes);
-        for (int h = 0; h < 2; ++h) {
-          if (pid[h] < 0) continue;
-          const int row = pid[h] * kPage;
-          for (int c = 0; c < 4; ++c)
-            tc::tma_load_2d(stage + c * kChunkBytes + h * (kChunkBytes / 2), tm_kv,
-                            &ctl->kv_full[st], c * 128, row);
-          tc::tma_load_2d(stage + 4 * kChunkBytes + h * (kRopeBytes / 2), tm_kvr,
-                          &ctl->kv_full[st], 512, row);
+      const int pid[2] = {pid0, pages == 2 ? pid1 : -1};
+      uint8_t* stage = smem + st * kStageBytes;
+      const int nbytes = ((pid[0] >= 0) + (pid[1] >= 0)) * kPageBytes;
+      if constexpr (!HALVES) {
+        // The stage is refilled, page by page, once PV of the tile two back is
+        // done (waited for above; one row block per item: the tile streams
+        // from HBM).
+        if (lane == 0 && !withhold) {
+          tc::mbar_arrive_expect_tx(&ctl->kv_full[st], nbytes);
+          for (int h = 0; h < 2; ++h) {
+            if (pid[h] < 0) continue;
+            const int row = pid[h] * kPage;
+            for (int c = 0; c < 4; ++c)
+              tc::tma_load_2d(stage + c * kChunkBytes + h * (kChunkBytes / 2), tm_kv,
+                              &ctl->kv_full[st], c * 128, row);
+            tc::tma_load_2d(stage + 4 * kChunkBytes + h * (kRopeBytes / 2), tm_kvr,
+                            &ctl->kv_full[st], 512, row);
+          }
         }
+        last_kv_parity[st] = withhold ? -1 : (int)((g >> 1) & 1);
+      } else {
+        // Several row blocks per item (their jobs share each tile through L2):
+        // the stage is refilled in two halves, value bands 0-1 and the rope
+        // (which only S reads) once PV of the tile two back is done with bands
+        // 0-1, bands 2-3 once that PV is done. kv_full is armed for the whole
+        // tile after the first wait, which proves the stage's previous phase
+        // completed (that PV ran on its data).
+        for (int part = 0; part < 2; ++part) {
+          if (g >= 2 &&
+              !(ok = wait0(part == 0 ? &ctl->pv_half[st] : &ctl->pv_done[st], ((g >> 1) - 1) & 1)))
+            break;
+          if (part == 0) {
+            if (lane == 0 && !withhold) tc::mbar_arrive_expect_tx(&ctl->kv_full[st], nbytes);
+            last_kv_parity[st] = withhold ? -1 : (int)((g >> 1) & 1);
+          }
+          if (lane == 0 && !withhold) {
+            for (int h = 0; h < 2; ++h) {
+              if (pid[h] < 0) continue;
+              const int row = pid[h] * kPage;
+              for (int c = 2 * part; c < 2 * part + 2; ++c)
+                tc::tma_load_2d(stage + c * kChunkBytes + h * (kChunkBytes / 2), tm_kv,
+                                &ctl->kv_full[st], c * 128, row);
+              if (part == 0)
+                tc::tma_load_2d(stage + 4 * kChunkBytes + h * (kRopeBytes / 2), tm_kvr,
+                                &ctl->kv_full[st], 512, row);
+            }
+          }
+        }
+        if (!ok) break;
       }
-      last_kv_parity[st] = withhold ? -1 : (int)((g >> 1) & 1);
       // Tile t + kStages is requested only once PV(t) frees this stage; warmed
       // in L2 now, its copy then skips most of the HBM latency.
       if (PREFETCH && t + kStages < jb.ntiles) {

@@ -141,7 +141,7 @@ __device__ __forceinline__ void tmem_st_rows(uint32_t taddr, const uint32_t (&r)
 }
 
 // ---------------------------------------------------------------- MMA issuer
-template <int NR>
+template <int NR, bool HALVES>
 __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_t tmem, int nb) {
   using C = Cfg<NR>;
   const uint32_t s_kv = tc::smem_u32(smem), s_q = tc::smem_u32(smem + C::kOffQ);
@@ -193,6 +193,8 @@ __device__ void mma_issuer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, uint32_
                        true);
         }
       }
+      // The producer refills bands 0-1 as soon as they are free (HALVES).
+      if constexpr (HALVES) if (dt == 1) tc::mma_commit(&ctl->pv_half[st]);
     }
     tc::mma_commit(&ctl->pv_done[st]);
   };
@@ -507,7 +509,9 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
   }
 }
 
-template <int NR>
+// HALVES: the work items have several row blocks, so sibling jobs share each
+// tile through L2 and a stage is refilled in two halves (decode_common.cuh).
+template <int NR, bool HALVES>
 __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
 decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
                  const __grid_constant__ CUtensorMap tm_kvr,
@@ -524,6 +528,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&ctl->kv_full[s], 1);
       tc::mbar_init(&ctl->pv_done[s], 1);
+      if (HALVES) tc::mbar_init(&ctl->pv_half[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->s_full[b], 1);
@@ -571,9 +576,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
   grid_dep_wait();      // the plan is complete; earlier readers of out/workspace are done
   grid_dep_launch();    // the reducer may launch; it still waits for this grid to finish
   if (warp == 0) {
-    producer<NR, Cfg<NR>::kOffQ, NR == 32, NR != 32>(a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr);
+    producer<NR, Cfg<NR>::kOffQ, NR == 32, NR != 32, HALVES>(a, smem, ctl, nb, &tm_kv, &tm_kvr,
+                                                            &tm_q, &tm_qr);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<NR>(a, smem, ctl, tmem, nb);
+    if (lane == 0) mma_issuer<NR, HALVES>(a, smem, ctl, tmem, nb);
   } else {
     softmax_epilogue<NR>(a, smem, ctl, tmem, nb);
   }
@@ -584,7 +590,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
 }
 
 // ---------------------------------------------------------------- host side
-template <int NR>
+template <int NR, bool HALVES>
 cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<NR>;
   CUtensorMap tkv, tkvr, tq, tqr;
@@ -601,7 +607,7 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
     return cudaErrorInvalidValue;
   const int smem_bytes = C::kOffCtl + (int)sizeof(Ctl) + 1024;
   static bool attr_set[64] = {};
-  cudaError_t e = set_smem(decode_tc_kernel<NR>, smem_bytes, attr_set);
+  cudaError_t e = set_smem(decode_tc_kernel<NR, HALVES>, smem_bytes, attr_set);
   if (e != cudaSuccess) return e;
   const int nb = row_blocks(a.M);
   const long long jobs = (long long)a.items * nb;
@@ -616,13 +622,14 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NR>, a, tkv, tkvr, tq, tqr, nb);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NR, HALVES>, a, tkv, tkvr, tq, tqr, nb);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
-  return row_block(a.M) == 32 ? launch_nr<32>(s, a, st) : launch_nr<64>(s, a, st);
+  if (row_block(a.M) == 32) return launch_nr<32, false>(s, a, st);
+  return row_blocks(a.M) > 1 ? launch_nr<64, true>(s, a, st) : launch_nr<64, false>(s, a, st);
 }
 
 }  // namespace mlafold
