@@ -101,10 +101,12 @@ typedef struct {
                                out and lse do not change. R * groups <= 1024.              */
 } mla_shape;
 
-/* Capacity, in entries, of the work list `work` that mla_plan_splits fills
- * for this shape: enough items for any length vector, plus two trailing
- * entries the decode uses as job counters (see mla_folded_decode). Returns
- * the capacity (>= 3) or a negative mla_status. Host only; launches nothing. */
+/* Length, in int32 words, of the plan buffer `work` that mla_plan_splits
+ * fills for this shape (layout at mla_plan_splits): E entries (E = units + R
+ * for the balanced policy, R x the uniform split count for the uniform one;
+ * units = num_ctas / ceil(M / row block), row block 32 for M <= 32 else 64),
+ * two job counters, 2E range words and 8 x units unit-table words. Returns
+ * the length or a negative mla_status. Host only; launches nothing. */
 int32_t mla_plan_list_len(const mla_shape *shape);
 
 /* Bytes of split-KV workspace mla_folded_decode and mla_split_combine need for
@@ -117,12 +119,32 @@ int32_t mla_workspace_bytes(const mla_shape *shape, size_t *bytes);
 
 /* Plan the step's splits on the device (one CTA), from the KV lengths.
  *   seq_lens [R] int32, device: keys per request (negative is read as 0).
- *   counts   [R*groups] int32, device, written: splits of each decode row group (>= 1).
- *   work     [list_len] int32, device, written: items (row group << 12 | split),
- *            row groups longest first (ties: lower index first), splits in
- *            ascending order, then -1 to the end. Row group g reads request
- *            g / groups.
+ *   counts   [R*groups] int32, device, written: pieces of each decode row group (>= 1).
+ *   work     [list_len] int32, device, written (-1 where unused, except as noted):
+ *            [0, E)      entries (row group << 12 | piece, plus 1 << 30 in
+ *                        every entry of a packed plan): row groups with two
+ *                        or more pieces first, then the others, each longest
+ *                        first (ties: lower index first), pieces in ascending
+ *                        order; a multi-piece entry's index is its partial slot.
+ *                        Row group g reads request g / groups.
+ *            [E, E+2)    the decode's job counters (-1).
+ *            [E+2, 3E+2) packed plans: entry e's first and end page within
+ *                        its row group's keys, at E+2+2e and E+3+2e.
+ *            [3E+2, ...) packed plans: 8 x units words, the entries each unit
+ *                        processes, in order, slot-major (unit u's j-th entry
+ *                        at 3E+2 + j * units + u; -1 padded).
+ *            Otherwise neither is written, and piece s of n covers pages
+ *            [floor(s p / n), floor((s+1) p / n)) of the row group's p pages.
+ *            Words past mla_plan_list_len(shape) are not written.
  *   list_len must be >= mla_plan_list_len(shape).
+ * Balanced policy: a chunk of c pages per split, c the even share of all pages
+ * over the units, raised until one wave of items fits when every request fits
+ * in one wave; equal page-aligned splits of each request. In that one-wave
+ * case, when the largest item would still exceed the even share by more than
+ * 1/8, the plan is packed instead: the row groups' pages, longest first, are
+ * laid end to end and cut into segments of the even share, one per unit
+ * (kept when no row group has more than max_splits pieces and no unit more
+ * than 8). Uniform policy: min(ceil(units / R), max_splits, pages) equal splits.
  * Integer arithmetic only; the result is a pure function of the lengths and
  * the shape (the project's CPU planner reproduces it bit for bit). */
 int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t *counts,
@@ -130,10 +152,12 @@ int32_t mla_plan_splits(const mla_shape *shape, const int32_t *seq_lens, int32_t
 
 /* Split-KV decode of the planned work list. Persistent CTAs take one job
  * each (a work item's block of query rows), then claim further jobs in list
- * order from a counter kept in the two entries after the items in `work`
+ * order from a counter kept in the two words after the entries in `work`
  * (the plan leaves them at -1; the decode counts them down and its last CTA
  * puts them back to -1), so one plan serves any number of decodes in stream
- * order. Decodes that share one `work` array must not run concurrently.
+ * order; with a packed plan CTA b (row block b % nb of unit b / nb,
+ * nb = ceil(M / row block)) walks unit b / nb's entries instead.
+ * Decodes that share one `work` array must not run concurrently.
  *   q           [R*k, H, 576] FP8 E4M3, device, 16-byte aligned: the queries in the
  *               stock token-major layout (= the folded [R, M, 576] view).
  *   kv          [num_pages, 64, 576] FP8 E4M3, device, 16-byte aligned: the

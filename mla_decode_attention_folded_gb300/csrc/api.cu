@@ -109,6 +109,9 @@ int32_t decode_impl(const mla_shape* shape, const void* q, const void* kv,
   a.counts = counts;
   a.work = work;
   a.sched = work + plan_items(*shape);
+  a.ranges = work + plan_ranges_offset(*shape);
+  a.units = work + plan_units_offset(*shape);
+  a.nunits = plan_units(M, shape->num_ctas);
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                     partial_out_bytes(slots, M))

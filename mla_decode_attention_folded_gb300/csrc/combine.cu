@@ -46,8 +46,8 @@ combine_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ w
     int r = 0;
     if (e < scan) {
       const int w = __ldcg(work + e);
-      if (w >= 0 && (w & ((1 << kSplitBits) - 1)) == 0) {
-        r = w >> kSplitBits;
+      if (w >= 0 && entry_split(w) == 0) {
+        r = entry_request(w);
         first = r < R && __ldcg(counts + r) >= 2;
       }
     }

@@ -77,13 +77,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ct
 
 
 
-__device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, bool report) {
+// A job of work-list entry `item`: its request, rows and keys. A packed plan
+// gives each entry's page range; the other plans split each request into
+// equal, page-aligned parts.
+__device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, bool packed,
+                                        bool report) {
   Job jb;
   jb.item = item;
   jb.blk = blk;
   jb.skip = false;
   const int e = a.work[item];
-  const int r = e >> kSplitBits, s = e & ((1 << kSplitBits) - 1);
+  // Only a packed plan's entries carry kPackedBit.
+  const int r = packed ? entry_request(e) : e >> kSplitBits, s = entry_split(e);
   jb.r = r;
   if (r >= a.R || s >= a.counts[r]) {
     if (report && a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
@@ -98,7 +103,17 @@ __device__ __forceinline__ Job read_job(const DecodeArgs& a, int item, int blk, 
     if (report && a.status) atomicOr(a.status, MLA_FAULT_PAGE_RANGE);
     L = a.max_pages * kPage;
   }
-  split_range(L, n, s, jb.j0, jb.j1);
+  if (!packed) {
+    split_range(L, n, s, jb.j0, jb.j1);
+  } else {
+    const int pa = a.ranges[2 * item], pb = a.ranges[2 * item + 1];
+    if (pa < 0 || pa > pb || (long long)pb > cdiv(L, kPage)) {
+      if (report && a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
+      jb.skip = true;
+    }
+    jb.j1 = min(L, max(pb, 0) * kPage);
+    jb.j0 = min(max(pa, 0) * kPage, jb.j1);
+  }
   jb.ntiles = (int)cdiv(jb.j1 - jb.j0, kTileKeys);
   jb.direct = n == 1;
   if (!jb.direct && item >= a.slots) {
@@ -174,11 +189,15 @@ __device__ __forceinline__ void finish_jobs(const DecodeArgs& a) {
 // offset of the Q block; STAGGER: request the CTA's second tile only once its
 // first has landed; PREFETCH: with each tile, warm L2 with the pages of the
 // tile that will next use the same stage; HALVES: refill a stage in two
-// halves (below).
-template <int QROWS, int OFFQ, bool STAGGER, bool PREFETCH, bool HALVES>
-__device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
-                         const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
-                         const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
+// halves (below); PACKED: the plan is packed (bit 30 of its entries); e0:
+// the entry of job blockIdx.x when the caller loaded it (E0), used for the
+// first job of a per-request plan instead of loading it again.
+template <int QROWS, int OFFQ, bool STAGGER, bool PREFETCH, bool HALVES, bool PACKED,
+          bool E0 = false>
+__device__ __forceinline__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
+                                         const CUtensorMap* tm_kv, const CUtensorMap* tm_kvr,
+                                         const CUtensorMap* tm_q, const CUtensorMap* tm_qr,
+                                         int e0 = -1) {
   constexpr int kQChunk = QROWS * 128, kQBytes = QROWS * kDqk;
   const int lane = threadIdx.x & 31;
   uint32_t g = 0, x = 0;
@@ -205,27 +224,37 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
     return p;
   };
   int job = (int)blockIdx.x;
+  // A packed plan (bit 30 of its entries) gives each unit a fixed list of
+  // entries, slot-major in its unit table: CTA b, row block b % nb of unit
+  // b / nb, takes jobs b, b + U nb, b + 2 U nb, ... through the table instead
+  // of claiming.
+  constexpr bool packed = PACKED;
+  const int stride = a.nunits * nb;
+  const int jobs_end = !packed ? njobs : (job < stride ? kUnitSlots * stride : 0);
+  bool first = E0;
   for (uint32_t seq = 0; ok; ++seq) {
     Job jb;
     int blk = 0;
     bool have = false;
-    while (job < njobs) {                        // the next job that is not malformed
-      const int item = job / nb;
+    while (job < jobs_end) {                     // the next job that is not malformed
+      int item = job / nb;
       blk = job % nb;
-      if (a.work[item] < 0) break;               // past the last item (the list is compact)
-      jb = read_job(a, item, blk, lane == 0);
+      if (packed && ((item = a.units[item]) < 0 || item >= a.items)) break;   // list ended
+      if ((first ? e0 : a.work[item]) < 0) break;   // past the last item (the list is compact)
+      first = false;
+      jb = read_job(a, item, blk, packed, lane == 0);
       if (!jb.skip) {
         have = true;
         break;
       }
-      job = claim_job(a, lane);
+      job = packed ? job + stride : claim_job(a, lane);
     }
     if (!have) jb.item = -1;
     int pub = 1;
     if (lane == 0) pub = publish_job(ctl, seq, jb, a.status) ? 1 : 0;
     if (!(ok = __shfl_sync(0xffffffffu, pub, 0) != 0) || !have) break;
     if (jb.ntiles == 0) {                        // an empty split: the softmax role writes it
-      job = claim_job(a, lane);
+      job = packed ? job + stride : claim_job(a, lane);
       continue;
     }
     int cur = fetch(jb, 0), nxt = fetch(jb, 1);
@@ -325,7 +354,7 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
     }
     if (!ok) break;
     ++x;
-    job = claim_job(a, lane);
+    job = packed ? job + stride : claim_job(a, lane);
   }
   if (lane == 0) finish_jobs(a);
   // Never leave with copies in flight into this CTA's shared memory.
@@ -340,6 +369,17 @@ __device__ void producer(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, int nb,
            tc::globaltimer_ns() - t0 < kTimeoutNs) {
     }
   }
+}
+
+// The packed plan's producer, kept out of line: the per-request plans' producer
+// (inlined into the kernel) stays as compact as it is without packing.
+template <int QROWS, int OFFQ, bool STAGGER, bool PREFETCH, bool HALVES>
+__device__ __noinline__ void producer_packed(const DecodeArgs& a, uint8_t* smem, Ctl* ctl,
+                                             int nb, const CUtensorMap* tm_kv,
+                                             const CUtensorMap* tm_kvr,
+                                             const CUtensorMap* tm_q, const CUtensorMap* tm_qr) {
+  producer<QROWS, OFFQ, STAGGER, PREFETCH, HALVES, true>(a, smem, ctl, nb, tm_kv, tm_kvr, tm_q,
+                                                         tm_qr);
 }
 
 // ---------------------------------------------------------------- P conversion

@@ -511,7 +511,8 @@ __device__ void softmax_epilogue(const DecodeArgs& a, uint8_t* smem, Ctl* ctl, u
 
 // HALVES: the work items have several row blocks, so sibling jobs share each
 // tile through L2 and a stage is refilled in two halves (decode_common.cuh).
-template <int NR, bool HALVES>
+// PACKABLE: the shape allows a packed plan, so the kernel checks for one.
+template <int NR, bool HALVES, bool PACKABLE>
 __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
 decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
                  const __grid_constant__ CUtensorMap tm_kvr,
@@ -576,8 +577,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
   grid_dep_wait();      // the plan is complete; earlier readers of out/workspace are done
   grid_dep_launch();    // the reducer may launch; it still waits for this grid to finish
   if (warp == 0) {
-    producer<NR, Cfg<NR>::kOffQ, NR == 32, NR != 32, HALVES>(a, smem, ctl, nb, &tm_kv, &tm_kvr,
-                                                            &tm_q, &tm_qr);
+    // The entry of job blockIdx.x says whether the plan is packed.
+    const int e0 =
+        PACKABLE && (int)blockIdx.x < a.items * nb ? a.work[blockIdx.x / nb] : -1;
+    if (PACKABLE && e0 >= 0 && (e0 & kPackedBit))
+      producer_packed<NR, Cfg<NR>::kOffQ, NR == 32, NR != 32, HALVES>(a, smem, ctl, nb, &tm_kv,
+                                                                      &tm_kvr, &tm_q, &tm_qr);
+    else
+      producer<NR, Cfg<NR>::kOffQ, NR == 32, NR != 32, HALVES, false, PACKABLE>(
+          a, smem, ctl, nb, &tm_kv, &tm_kvr, &tm_q, &tm_qr, e0);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer<NR, HALVES>(a, smem, ctl, tmem, nb);
   } else {
@@ -590,7 +598,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_kv,
 }
 
 // ---------------------------------------------------------------- host side
-template <int NR, bool HALVES>
+template <int NR, bool HALVES, bool PACKABLE>
 cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<NR>;
   CUtensorMap tkv, tkvr, tq, tqr;
@@ -607,7 +615,7 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
     return cudaErrorInvalidValue;
   const int smem_bytes = C::kOffCtl + (int)sizeof(Ctl) + 1024;
   static bool attr_set[64] = {};
-  cudaError_t e = set_smem(decode_tc_kernel<NR, HALVES>, smem_bytes, attr_set);
+  cudaError_t e = set_smem(decode_tc_kernel<NR, HALVES, PACKABLE>, smem_bytes, attr_set);
   if (e != cudaSuccess) return e;
   const int nb = row_blocks(a.M);
   const long long jobs = (long long)a.items * nb;
@@ -622,14 +630,21 @@ cudaError_t launch_nr(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NR, HALVES>, a, tkv, tkvr, tq, tqr, nb);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NR, HALVES, PACKABLE>, a, tkv, tkvr, tq, tqr,
+                            nb);
+}
+
+template <bool PACKABLE>
+cudaError_t launch_kind(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
+  if (row_block(a.M) == 32) return launch_nr<32, false, PACKABLE>(s, a, st);
+  return row_blocks(a.M) > 1 ? launch_nr<64, true, PACKABLE>(s, a, st)
+                             : launch_nr<64, false, PACKABLE>(s, a, st);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const mla_shape& s, const DecodeArgs& a, cudaStream_t st) {
-  if (row_block(a.M) == 32) return launch_nr<32, false>(s, a, st);
-  return row_blocks(a.M) > 1 ? launch_nr<64, true>(s, a, st) : launch_nr<64, false>(s, a, st);
+  return plan_packable(s) ? launch_kind<true>(s, a, st) : launch_kind<false>(s, a, st);
 }
 
 }  // namespace mlafold

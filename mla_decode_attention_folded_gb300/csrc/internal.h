@@ -15,6 +15,11 @@ constexpr int kPage = 64;          // tokens per cache page
 constexpr int kDqk = 576;          // latent 512 + rope 64 (bytes per FP8 row)
 constexpr int kDv = 512;           // value = latent slice
 constexpr int kSplitBits = 12;     // work item = request << 12 | split
+constexpr int kPackedBit = 1 << 30;   // set in every entry of a packed plan
+__host__ __device__ inline int entry_request(int e) {
+  return (e & ~kPackedBit) >> kSplitBits;
+}
+__host__ __device__ inline int entry_split(int e) { return e & ((1 << kSplitBits) - 1); }
 constexpr int kMaxR = 1024;        // the planner runs one CTA with one thread per request
 constexpr int kMaxM = 4096;
 
@@ -45,11 +50,27 @@ inline int plan_items(const mla_shape& s) {
   if (s.policy == MLA_POLICY_BALANCED) return plan_units(M, s.num_ctas) + R;
   return R * uniform_splits(R, M, s.num_ctas, s.max_splits);
 }
-// After the items, the decode's two job counters (claimed jobs, finished
-// CTAs): the plan sets them to -1 with the rest of the padding, they count
-// down during a decode, and its last CTA sets them back to -1.
+// The plan buffer: the E entries, then the decode's two job counters (claimed
+// jobs, finished CTAs: the plan sets them to -1 with the rest of the padding,
+// they count down during a decode, and its last CTA sets them back to -1),
+// then each entry's first and end page within its request, then the packed
+// plan's per-unit piece table (kUnitSlots entries per unit, all -1 when the
+// plan is not packed).
 constexpr int kSchedWords = 2;
-inline int plan_list_len(const mla_shape& s) { return plan_items(s) + kSchedWords; }
+constexpr int kUnitSlots = 8;          // pieces a unit of a packed plan may hold
+constexpr int kMaxPackedUnits = 1024;  // the planner's per-unit tables
+// Whether the plan of this shape may be packed (the planner packs only then):
+// items of several row blocks, at most one request per unit.
+inline bool plan_packable(const mla_shape& s) {
+  const int M = group_rows(s), U = plan_units(M, s.num_ctas);
+  return s.policy == MLA_POLICY_BALANCED && row_blocks(M) >= 2 && plan_rows(s) <= U &&
+         U <= kMaxPackedUnits;
+}
+inline int plan_ranges_offset(const mla_shape& s) { return plan_items(s) + kSchedWords; }
+inline int plan_units_offset(const mla_shape& s) { return 3 * plan_items(s) + kSchedWords; }
+inline int plan_list_len(const mla_shape& s) {
+  return plan_units_offset(s) + kUnitSlots * plan_units(group_rows(s), s.num_ctas);
+}
 // Bound on items of multi-split requests; they occupy work-list slots [0, slots).
 inline int partial_slots(const mla_shape& s) {
   const int R = plan_rows(s), M = group_rows(s);
@@ -60,15 +81,6 @@ inline int partial_slots(const mla_shape& s) {
   int u = uniform_splits(R, M, s.num_ctas, s.max_splits);
   return u >= 2 ? R * u : 0;
 }
-inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-// Workspace: FP32 partial outputs [slots][M][512], then FP32 LSEs [slots][M].
-inline size_t partial_out_bytes(int slots, int M) { return align256(size_t(slots) * M * kDv * 4); }
-inline size_t workspace_bytes(const mla_shape& s) {
-  int slots = partial_slots(s), M = group_rows(s);
-  if (slots == 0) return 0;
-  return partial_out_bytes(slots, M) + align256(size_t(slots) * M * 4);
-}
-
 // Keys [j0, j1) of split s of n of a request of L keys (page-aligned cuts).
 __host__ __device__ inline void split_range(int L, int n, int s, int& j0, int& j1) {
   long long p = cdiv(L, kPage);
@@ -76,6 +88,14 @@ __host__ __device__ inline void split_range(int L, int n, int s, int& j0, int& j
   j0 = (int)(kPage * p0);
   long long e = kPage * p1;
   j1 = (int)(e < L ? e : L);
+}
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// Workspace: FP32 partial outputs [slots][M][512], then FP32 LSEs [slots][M].
+inline size_t partial_out_bytes(int slots, int M) { return align256(size_t(slots) * M * kDv * 4); }
+inline size_t workspace_bytes(const mla_shape& s) {
+  int slots = partial_slots(s), M = group_rows(s);
+  if (slots == 0) return 0;
+  return partial_out_bytes(slots, M) + align256(size_t(slots) * M * 4);
 }
 
 struct DecodeArgs {
@@ -86,6 +106,8 @@ struct DecodeArgs {
   const int32_t* counts;
   const int32_t* work;
   int32_t* sched;    // work + items: the job counters
+  const int32_t* ranges;   // each entry's first and end page within its request
+  const int32_t* units;    // packed plan: unit u's entry k at k * nunits + u
   float* part_o;     // [slots][M][512]
   float* part_lse;   // [slots][M]
   uint16_t* out;     // [R][M][512] bf16 bits
@@ -94,6 +116,7 @@ struct DecodeArgs {
   float bmm1_log2;   // bmm1_scale * log2(e)
   float bmm2;
   int R, M, max_pages, num_pages, items, slots;   // R, M: row groups, rows per group
+  int nunits;          // units of the plan (its unit table's rows)
   int groups;          // row group g reads request g / groups
   unsigned long long wait_limit_ns;   // bound of every pipeline wait (drains keep their own)
   int withhold_first_copy;            // failure-detection test: CTA 0 never issues its

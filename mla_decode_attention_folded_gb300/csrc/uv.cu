@@ -256,8 +256,8 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
   const int scan = min(a.list_len, a.slots);
   for (int e = threadIdx.x; e + 1 < scan; e += blockDim.x) {
     const int w = __ldcg(a.work + e);
-    if (w >= 0 && (w & ((1 << kSplitBits) - 1)) == 0 && __ldcg(a.work + e + 1) == w + 1) {
-      const int r = w >> kSplitBits;
+    if (w >= 0 && entry_split(w) == 0 && __ldcg(a.work + e + 1) == w + 1) {
+      const int r = entry_request(w);
       if (r < a.plan_rows) s_start[r] = e;
     }
   }

@@ -12,15 +12,6 @@ from mla_decode_attention_folded_gb300 import _lib
 from oracle import planner as pl
 
 HEADER = os.path.join(os.path.dirname(__file__), "..", "include", "mlafold.h")
-# The library's work list holds the plan's items and, after them, two entries
-# the decode uses as job counters (the plan sets them to -1 like the padding).
-SCHED_WORDS = 2
-
-
-def library_len(items):
-    return items + SCHED_WORDS
-
-
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -52,7 +43,7 @@ def test_noalloc_limit_matches_header():
 def test_sizes_match_oracle_planner(R, k, H, G, policy, ms):
     s = mla.make_shape(R, k, H, 10, 100, G, 256, ms, policy)
     M = k * H
-    assert mla.plan_list_len(s) == library_len(pl.list_len(R, M, G, policy, ms))
+    assert mla.plan_list_len(s) == pl.list_len(R, M, G, policy, ms)
     slots = pl.partial_slots(R, M, G, policy, ms)
     align = lambda x: (x + 255) // 256 * 256
     want = 0 if slots == 0 else align(slots * M * 512 * 4) + align(slots * M * 4)
@@ -109,7 +100,7 @@ def test_row_group_sizes_match_oracle(R, k, H, groups):
     for policy in (pl.BALANCED, pl.UNIFORM):
         s = mla.make_shape(R, k, H, 10, 100, 152, 256, 64, policy, groups)
         Rg, Mg = R * groups, (k // groups) * H
-        assert mla.plan_list_len(s) == library_len(pl.list_len(Rg, Mg, 152, policy, 64))
+        assert mla.plan_list_len(s) == pl.list_len(Rg, Mg, 152, policy, 64)
         slots = pl.partial_slots(Rg, Mg, 152, policy, 64)
         align = lambda x: (x + 255) // 256 * 256
         want = 0 if slots == 0 else align(slots * Mg * 512 * 4) + align(slots * Mg * 4)

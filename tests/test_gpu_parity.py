@@ -31,6 +31,18 @@ def _gpu_plan(lens, M, G, mst, ms, policy):
     return counts.cpu().numpy(), work.cpu().numpy()
 
 
+def _same_plan(c, wk, c2, wk2, R, M, G, policy, ms):
+    """Device plan == CPU plan: counts, entries and counters always; ranges
+    and unit table when the plan is packed (the device planner leaves them
+    unwritten otherwise)."""
+    E, off_rng, off_unit = pl.regions(R, M, G, policy, ms)
+    if not (np.array_equal(c, c2) and np.array_equal(wk[:off_rng], wk2[:off_rng])):
+        return False
+    if int(wk2[0]) >= 0 and int(wk2[0]) & pl.PACKED_BIT:
+        return np.array_equal(wk[off_rng:], wk2[off_rng:])
+    return True
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS))
 @pytest.mark.parametrize("policy", [pl.BALANCED, pl.UNIFORM])
 def test_planner_bit_exact_on_workloads(name, policy):
@@ -42,7 +54,7 @@ def test_planner_bit_exact_on_workloads(name, policy):
     for G in (8, _sms()):
         c, wk = _gpu_plan(lens, w.M, G, 256, 64, policy)
         c2, wk2 = pl.plan(lens, w.M, G, 256, 64, policy, capacity=len(wk))
-        assert np.array_equal(c, c2) and np.array_equal(wk, wk2)
+        assert _same_plan(c, wk, c2, wk2, len(lens), w.M, G, policy, 64)
 
 
 def test_planner_bit_exact_random():
@@ -66,8 +78,7 @@ def test_planner_bit_exact_random():
         policy = int(rng.integers(0, 2))
         c, wk = _gpu_plan(lens, M, G, mst, ms, policy)
         c2, wk2 = pl.plan(lens, M, G, mst, ms, policy, capacity=len(wk))
-        assert np.array_equal(c, c2), (trial, R, M, G)
-        assert np.array_equal(wk, wk2), (trial, R, M, G)
+        assert _same_plan(c, wk, c2, wk2, R, M, G, policy, ms), (trial, R, M, G)
 
 
 # ---------------------------------------------------------------- decode
@@ -134,8 +145,8 @@ def test_planner_bit_exact_with_row_groups():
         mla.plan_splits(s, torch.tensor(lens.astype(np.int32), device="cuda"), counts, work)
         c2, w2 = pl.plan(np.repeat(lens, groups), (k // groups) * H, G, 256, 64, policy,
                          capacity=n)
-        assert np.array_equal(counts.cpu().numpy(), c2), trial
-        assert np.array_equal(work.cpu().numpy(), w2), trial
+        assert _same_plan(counts.cpu().numpy(), work.cpu().numpy(), c2, w2, R * groups,
+                          (k // groups) * H, G, policy, 64), trial
 
 
 @pytest.mark.parametrize("lens,k,H", [((900, 77, 2000), 4, 64), ((1500, 300), 7, 8),
@@ -239,7 +250,8 @@ def test_claimed_jobs_and_repeated_decodes_of_one_plan(lens, k, H, G, groups, po
     eng.plan(d["lens"])
     torch.cuda.synchronize()
     planned = eng.work.cpu().clone()
-    assert torch.all(planned[-2:] == -1)
+    E = pl.items_len(b.R * groups, (k // groups) * H, G, policy, 64)
+    assert torch.all(planned[E:E + 2] == -1)                # the job counters
     runs = []
     for _ in range(3):
         out, lse = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2)
@@ -252,6 +264,49 @@ def test_claimed_jobs_and_repeated_decodes_of_one_plan(lens, k, H, G, groups, po
     ref_o, ref_l = oracle_full(b)
     assert_close(runs[0][0].float().cpu(), runs[0][1].cpu(), ref_o, ref_l,
                  f"lens={len(lens)} requests k={k} H={H} G={G} groups={groups} policy={policy}")
+
+
+@pytest.mark.parametrize("lens,k,H,G,groups", [
+    ((2625, 797, 6485, 1686), 2, 64, 10, 1),                # two 64-row blocks per item
+    ((5400, 0, 4962, 1294, 6586), 2, 64, 11, 1),            # two blocks, an empty request
+    ((3000, 2500, 2000, 1500), 4, 64, 16, 1),               # four blocks
+    ((9000, 4000, 0, 0, 2000, 64, 1), 7, 64, 56, 1),        # seven blocks, empty requests
+    ((258, 4369, 1331, 3613), 4, 64, 25, 2),                # row groups of two blocks
+    ((0, 5322, 7175, 1472), 4, 64, 22, 2),                  # row groups, an empty request
+])
+def test_packed_plans(lens, k, H, G, groups):
+    """Batches of at most one request per unit whose per-request plan leaves
+    one large item, with several row blocks per item: the plan packs the
+    rank-ordered pages into equal segments and each unit's CTAs walk their own
+    entries. The device plan equals the oracle's bit for bit, three
+    decodes of it agree bit for bit and with the oracle, and the buffer is left
+    as planned."""
+    b = make_batch_from_lengths(lens, k, H, seed=sum(lens) + G + 5, scaling="amax")
+    rows = np.repeat(np.asarray(lens), groups)
+    M = (k // groups) * H
+    want_counts, want_buf = pl.plan(rows, M, G, 64, 64, pl.BALANCED)
+    assert int(want_buf[0]) & pl.PACKED_BIT, "the case must give a packed plan"
+    d = to_device(b)
+    eng = mla.FoldedMla(b.R, b.k, b.H, d["bt"].shape[1], d["kv"].shape[0], "cuda", num_ctas=G,
+                        min_split_tokens=64, groups=groups)
+    bmm1, bmm2 = bmm_scales(b)
+    eng.plan(d["lens"])
+    torch.cuda.synchronize()
+    planned = eng.work.cpu().clone()
+    assert _same_plan(eng.counts.cpu().numpy(), planned.numpy(), want_counts, want_buf,
+                      len(rows), M, G, pl.BALANCED, 64)
+    runs = []
+    for _ in range(3):
+        out, lse = eng.decode(d["q"], d["kv"], d["bt"], d["lens"], bmm1, bmm2)
+        torch.cuda.synchronize()
+        assert torch.equal(eng.work.cpu(), planned)
+        runs.append((out.clone(), lse.clone()))
+    assert int(eng.status.item()) == 0
+    for o, l in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
+    ref_o, ref_l = oracle_full(b)
+    assert_close(runs[0][0].float().reshape(b.R, b.M, 512).cpu(), runs[0][1].reshape(b.R, b.M).cpu(),
+                 ref_o, ref_l, f"packed {lens} k={k} H={H} G={G} groups={groups}")
 
 
 def test_out_of_range_page_sets_status_without_fault():
@@ -395,11 +450,11 @@ def test_combine_on_oracle_partials():
     for idx, e in enumerate(work):
         if e < 0:
             break
-        r, sp = int(e) >> 12, int(e) & 4095
+        r = pl.entry_request(e)
         if counts[r] < 2:
             continue
         kr = np.zeros((b.R, 2), dtype=np.int64)
-        kr[r] = pl.split_range(int(lens[r]), int(counts[r]), sp)
+        kr[r] = pl.entry_keys(work, counts, idx, int(lens[r]), b.R, b.M, G, pl.BALANCED, 64)
         o, l = att.mla_decode(b.q.numpy(), b.kv.numpy(), b.block_table.numpy(), lens, b.k,
                               b.sm_scale, b.q_scale, b.kv_scale, key_range=kr, requests=[r])
         po[idx] = torch.from_numpy(o.reshape(b.R, b.M, 512)[r] / b.kv_scale).float()

@@ -99,11 +99,11 @@ def test_uv_on_oracle_partials():
     for idx, e in enumerate(work):
         if e < 0:
             break
-        r, sp = int(e) >> 12, int(e) & 4095
+        r = pl.entry_request(e)
         if counts[r] < 2:
             continue
         kr = np.zeros((b.R, 2), dtype=np.int64)
-        kr[r] = pl.split_range(int(lens[r]), int(counts[r]), sp)
+        kr[r] = pl.entry_keys(work, counts, idx, int(lens[r]), b.R, b.M, G, pl.BALANCED, 64)
         o, l = att.mla_decode(b.q.numpy(), b.kv.numpy(), b.block_table.numpy(), lens, b.k,
                               b.sm_scale, b.q_scale, b.kv_scale, key_range=kr, requests=[r])
         po[idx] = torch.from_numpy(o.reshape(b.R, b.M, 512)[r] / b.kv_scale).float()
