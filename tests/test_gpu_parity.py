@@ -57,6 +57,21 @@ def test_planner_bit_exact_on_workloads(name, policy):
         assert _same_plan(c, wk, c2, wk2, len(lens), w.M, G, policy, 64)
 
 
+@pytest.mark.parametrize("lens,M,G", [
+    ([6390, 5100, 3800], 256, 16),                                  # packed worked example
+    ([0, 13474, 4345, 6990, 0, 0, 3742, 4383], 256, 44),            # packed, empty requests
+    ([1021, 1786, 3049, 5808, 5645, 717, 3996, 4808, 2938], 128, 29),   # kept by the cost
+    ([16384, 40000, 65536, 30000] * 4, 256, 152),                   # packed, 16 requests
+])
+def test_planner_bit_exact_on_packing_pins(lens, M, G):
+    """The device planner takes the packing decision and lays out a packed
+    plan exactly as the CPU planner's pinned cases do."""
+    c, wk = _gpu_plan(lens, M, G, 64, 64, pl.BALANCED)
+    c2, wk2 = pl.plan(lens, M, G, 64, 64, pl.BALANCED, capacity=len(wk))
+    assert _same_plan(c, wk, c2, wk2, len(lens), M, G, pl.BALANCED, 64)
+    assert bool(int(wk[0]) & pl.PACKED_BIT) == bool(int(wk2[0]) & pl.PACKED_BIT)
+
+
 def test_planner_bit_exact_random():
     rng = np.random.default_rng(123)
     for trial in range(2000):

@@ -222,6 +222,43 @@ def test_packed_plans_balance_one_wave_batches(seed):
         assert [int((row >= 0).sum()) for row in table[:nseg]] == per_unit
 
 
+def test_packed_plan_places_empty_requests():
+    """A packed plan gives the k-th empty request (in rank order, that is by
+    index) one empty piece in unit k mod (number of segments), after that
+    unit's non-empty pieces."""
+    lens = [0, 13474, 4345, 6990, 0, 0, 3742, 4383]
+    M, G = 256, 44                              # four 64-row blocks, U = 11
+    counts, buf = pl.plan(lens, M, G, 64, 64, pl.BALANCED)
+    E, entries, rng, table = _unpack(buf, len(lens), M, G, pl.BALANCED, 64)
+    assert int(entries[0]) & pl.PACKED_BIT
+    p = [-(-L // 64) for L in lens]
+    c0 = -(-sum(p) // pl.units(M, G))
+    nseg = -(-sum(p) // c0)
+    empties = [0, 4, 5]
+    for k, i in enumerate(empties):
+        e = [j for j in range(E) if entries[j] >= 0 and pl.entry_request(entries[j]) == i]
+        assert len(e) == 1 and tuple(rng[e[0]]) == (0, 0)
+        row = [x for x in table[k % nseg] if x >= 0]
+        slot = row.index(e[0])
+        assert all(pl.entry_request(entries[x]) not in empties for x in row[:slot])
+        assert all(pl.entry_request(entries[x]) in empties for x in row[slot:])
+
+
+def test_packing_cost_keeps_the_per_request_plan():
+    """The unit cost decides: nine requests of 1021 .. 5808 keys, M = 128 (two
+    row blocks), 29 CTAs: U = 14, pages 16 28 48 91 89 12 63 76 46 (T = 469),
+    c0 = 34; the per-request plan's largest item is 46 pages, so
+    8 (c0 + 2 J) = 336 <= 7 (46 + J) = 350 lets packing be tried, but segment
+    12 ([408, 442), full) would hold three pieces: cost >= 34 + 3 J = 46 and
+    8 * 46 = 368 > 350, so the per-request plan stands."""
+    lens = [1021, 1786, 3049, 5808, 5645, 717, 3996, 4808, 2938]
+    assert pl.JOB_PAGES == 4
+    _, packed = pl.plan_pieces(lens, 128, 29, 64, 64, pl.BALANCED)
+    assert not packed
+    counts, buf = pl.plan(lens, 128, 29, 64, 64, pl.BALANCED)
+    assert not int(buf[0]) & pl.PACKED_BIT
+
+
 def test_empty_and_degenerate():
     counts, work = pl.plan([0, 0, 0], 32, 152, 256, 64, pl.BALANCED)
     assert counts.tolist() == [1, 1, 1]
