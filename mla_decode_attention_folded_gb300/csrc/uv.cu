@@ -11,12 +11,15 @@
 // N ("swap-AB": 32 tokens keep even the smallest batches spread over SMs):
 //     Y^T[128, 32] = W_UV[h]^T[128, 512] . X[32, 512]^T,  8 chunks x 4 MMAs (K = 16)
 // W_UV[h] (128 KB) stays in shared memory while the CTA's tiles share a head.
-// X, a tile's 32 merged BF16 rows, is built in shared memory by 256 reducer
-// threads (8 per token row, interleaved 16-byte pieces): from the decode's own BF16
-// row for a request with one split, else from the FP32 split partials and
-// their LSEs. X and the TMEM accumulator are double-buffered, so a tile's
-// reduction overlaps the previous tile's MMAs and the read-back of the one
-// before; four of the reducer warps read the accumulator back and store Y.
+// X, a tile's 32 merged BF16 rows, lands in shared memory by TMA from the
+// decode's own BF16 rows (the rows of a request with one split; viewed as
+// [token][head][512] they form one box per 64-dim chunk), issued one tile
+// ahead; then 256 reducer threads (8 per token row, interleaved 16-byte
+// pieces) overwrite the rows of requests with several splits with their merge
+// of the FP32 split partials. X and the TMEM accumulator are double-buffered,
+// so a tile's loads and merges overlap the previous tile's MMAs and the
+// read-back of the one before; four of the reducer warps read the
+// accumulator back and store Y.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -49,7 +52,8 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 struct UvCtl {
   uint64_t w_full[kChunks];   // TMA -> MMA: W chunk landed (one phase per head loaded)
-  uint64_t x_full[2];         // reducers -> MMA: X buffer written
+  uint64_t x_full[2];         // reducers -> MMA: X buffer's merged rows written
+  uint64_t x_tma[2];          // TMA -> reducers, MMA: X buffer's one-split rows landed
   uint64_t x_empty[2];        // MMA -> reducers (and W reload): the tile's MMAs finished
   uint64_t d_full[2];         // MMA -> read-back: accumulator final
   uint64_t d_empty[2];        // read-back -> MMA: accumulator read
@@ -92,13 +96,13 @@ __device__ __forceinline__ int x_piece(int row, int i) {
   return (i >> 3) * kXChunk + row * 128 + (((i & 7) ^ (row & 7)) << 4);
 }
 
-// Writes one token row's merged BF16 latent output into X. The 8 threads of the
-// row (consecutive lanes; this one is `c`) cover it interleaved: thread c takes
-// the 16-byte pieces 8 v + c (v = 0..7) of the BF16 row, or the float4s
-// 8 v + c (v = 0..15) of an FP32 partial row, so that each warp-wide load
-// reads whole 128-byte lines.
+// Writes one token row's merged BF16 latent output into X when the row's
+// request has several splits (the tile's TMA load brings the other rows). The
+// 8 threads of the row (consecutive lanes; this one is `c`) cover it
+// interleaved: thread c takes the float4s 8 v + c (v = 0..15) of an FP32
+// partial row, so that each warp-wide load reads whole 128-byte lines.
 // `ready()` is called once, after the row's global loads and before its first
-// shared-memory write (it waits for the X buffer to be free); false = give up.
+// shared-memory write (it waits for the tile's TMA load); false = give up.
 template <typename Ready>
 __device__ __forceinline__ bool merged_row(const UvArgs& a, const int* s_start,
                                            const int* s_count, int tau, int h,
@@ -113,23 +117,12 @@ __device__ __forceinline__ bool merged_row(const UvArgs& a, const int* s_start,
     mg = (t % kg) * a.H + h;                    // its row within that group
     n = s_count[i];
   }
-  if (tau >= a.T) {                             // rows past the batch stay zero
-    if (!ready()) return false;
-#pragma unroll
-    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(x + x_piece(row, 8 * v + c)) = zero;
-    return true;
-  }
-  if (n <= 1) {                                 // one split: the decode's BF16 row
-    const uint4* src = reinterpret_cast<const uint4*>(
-        a.out + ((size_t)r * a.M + (size_t)t * a.H + h) * kDv);
-    uint4 v8[8];
-#pragma unroll
-    for (int v = 0; v < 8; ++v) v8[v] = src[8 * v + c];
-    if (!ready()) return false;
-#pragma unroll
-    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(x + x_piece(row, 8 * v + c)) = v8[v];
-    return true;
-  }
+  // Rows past the batch (zero filled) and one-split rows come with the tile's
+  // TMA load. Every thread still waits for it (ready()) before it arrives on
+  // x_full: that load follows the MMAs of the tile two back, so no thread
+  // arrives for a tile before the barrier's phase of the tile two back is
+  // complete.
+  if (tau >= a.T || n <= 1) return ready();
   const int start = s_start[i];
   if (start < 0 || start + n > a.slots) {       // not a plan of this shape: leave zeros
     if (a.status) atomicOr(a.status, MLA_FAULT_WORK_ITEM);
@@ -199,7 +192,8 @@ __device__ __forceinline__ bool merged_row(const UvArgs& a, const int* s_start,
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
+uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w,
+          const __grid_constant__ CUtensorMap tm_x) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -217,6 +211,7 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
     for (int c = 0; c < kChunks; ++c) tc::mbar_init(&ctl->w_full[c], 1);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->x_full[b], kRed);
+      tc::mbar_init(&ctl->x_tma[b], 1);
       tc::mbar_init(&ctl->x_empty[b], 1);
       tc::mbar_init(&ctl->d_full[b], 1);
       tc::mbar_init(&ctl->d_empty[b], 128);
@@ -226,7 +221,10 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
     tc::fence_barrier_init();
   }
   if (warp == 0) {
-    if (lane == 0) tc::prefetch_tmap(&tm_w);
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_w);
+      tc::prefetch_tmap(&tm_x);
+    }
     tc::tmem_alloc(&ctl->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -271,8 +269,30 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
       bool ok = true;
       bool w_ready = false;
       int it = 0;
+      // The one-split rows of tile `tile` into X buffer `b` (eight 64-dim chunks).
+      auto load_x = [&](int tile, int b) {
+        const int h = tile / nblk, tok0 = (tile % nblk) * kTok;
+        tc::mbar_arrive_expect_tx(&ctl->x_tma[b], kXBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tc::tma_load_3d(smem + kOffX + b * kXBytes + c * kXChunk, &tm_x, &ctl->x_tma[b],
+                          c * 128, h, tok0);
+      };
+      int x_loads = 0;                         // tiles whose X load was issued
+      if (t_begin < t_end) {
+        load_x(t_begin, 0);
+        x_loads = 1;
+      }
       for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
         const int h = tile / nblk, buf = it & 1;
+        // The next tile's X goes to the other buffer once the MMAs of the
+        // tile before this one (its last reader) are done.
+        if (tile + 1 < t_end) {
+          if (it >= 1 &&
+              !(ok = uv_wait(&ctl->x_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, ctl, a.status)))
+            break;
+          load_x(tile + 1, (it + 1) & 1);
+          x_loads = it + 2;
+        }
         if (h != cur_h) {
           // The previous tile's MMAs must be done reading W before it is replaced.
           if (it > 0 &&
@@ -287,6 +307,7 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
           cur_h = h;
           w_ready = false;
         }
+        if (!(ok = uv_wait(&ctl->x_tma[buf], (it >> 1) & 1, ctl, a.status))) break;
         if (!(ok = uv_wait(&ctl->x_full[buf], (it >> 1) & 1, ctl, a.status))) break;
         if (it >= 2 &&
             !(ok = uv_wait(&ctl->d_empty[buf], ((it - 2) >> 1) & 1, ctl, a.status)))
@@ -317,6 +338,10 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
             while (!tc::mbar_try_wait(&ctl->w_full[c], (loads - 1) & 1) &&
                    tc::globaltimer_ns() - t0 < kTimeoutNs) {
             }
+        for (int j = x_loads - 2 < 0 ? 0 : x_loads - 2; j < x_loads; ++j)
+          while (!tc::mbar_try_wait(&ctl->x_tma[j & 1], (j >> 1) & 1) &&
+                 tc::globaltimer_ns() - t0 < kTimeoutNs) {
+          }
         while (!tc::mbar_try_wait(&ctl->drain, 0) && tc::globaltimer_ns() - t0 < kTimeoutNs) {
         }
       }
@@ -347,12 +372,11 @@ uv_kernel(const UvArgs a, const __grid_constant__ CUtensorMap tm_w) {
     int it = 0;
     for (int tile = t_begin; tile < t_end; ++tile, ++it) {
       const int h = tile / nblk, tok0 = (tile % nblk) * kTok, buf = it & 1;
-      // X[buf] is free once the MMAs of the tile two back have read it: wait
-      // for that only after the row's loads are in flight.
+      // A merged row overwrites the tile's TMA-loaded one: wait for that load
+      // (issued once X[buf] was free) only after the row's loads are in flight.
       const int it_now = it;
       auto x_free = [&]() {
-        return it_now < 2 ||
-               uv_wait(&ctl->x_empty[it_now & 1], ((it_now - 2) >> 1) & 1, ctl, a.status);
+        return uv_wait(&ctl->x_tma[it_now & 1], (it_now >> 1) & 1, ctl, a.status);
       };
       if (!(ok = merged_row(a, s_start, s_count, tok0 + row, h, c, smem + kOffX + buf * kXBytes, row,
                             x_free)))
@@ -402,6 +426,17 @@ cudaError_t launch_uv(const mla_shape& s, const int32_t* counts, const int32_t* 
          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // The decode's BF16 rows as [token][head][512]: one box = 32 tokens x 64
+  // dims (128 bytes) of one head, rows past the batch zero filled.
+  CUtensorMap tmx;
+  const cuuint64_t xdims[3] = {(cuuint64_t)kDv * 2, (cuuint64_t)s.H,
+                               (cuuint64_t)s.R * s.k};
+  const cuuint64_t xstrides[2] = {(cuuint64_t)kDv * 2, (cuuint64_t)s.H * kDv * 2};
+  const cuuint32_t xbox[3] = {128, 1, kTok}, xes[3] = {1, 1, 1};
+  if (fn(&tmx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint16_t*>(out), xdims, xstrides,
+         xbox, xes, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -440,7 +475,7 @@ cudaError_t launch_uv(const mla_shape& s, const int32_t* counts, const int32_t* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, uv_kernel, a, tm);
+  return cudaLaunchKernelEx(&cfg, uv_kernel, a, tm, tmx);
 }
 
 }  // namespace mlafold
