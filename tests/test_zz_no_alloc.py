@@ -53,6 +53,24 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row():
         assert_close(o.float().numpy(), l.numpy(), ref_o, ref_l, "no-alloc vs oracle")
 
 
+def test_noalloc_on_a_packed_plan():
+    """Eleven requests of 256 rows (four row blocks) on every SM: the plan packs
+    the requests' pages into equal per-unit segments; the allocation-free call
+    and the regular one agree bit for bit and with the oracle."""
+    from oracle import planner as pl
+    lens = (13435, 22970, 14236, 18445, 2082, 8967, 5989, 10509, 4787, 11033, 22350)
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    _, packed = pl.plan_pieces(lens, 256, G, 64, 64, pl.BALANCED)
+    if not packed:
+        pytest.skip("this device's SM count does not pack the batch")
+    b = make_batch_from_lengths(lens, 4, 64, seed=303, scaling="amax")
+    (ro, rl), (o, l) = _decode_both(b)
+    assert torch.equal(o.view(torch.int16), ro.view(torch.int16)), "out differs"
+    assert torch.equal(l, rl), "lse differs"
+    ref_o, ref_l = oracle_full(b)
+    assert_close(o.float().numpy(), l.numpy(), ref_o, ref_l, "no-alloc, packed plan")
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     # Every device pointer is NULL: a working size check returns
     # MLA_ERR_SCRATCH_LIMIT first; were it missing, the null checks of the
