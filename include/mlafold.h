@@ -102,11 +102,12 @@ typedef struct {
 } mla_shape;
 
 /* Length, in int32 words, of the plan buffer `work` that mla_plan_splits
- * fills for this shape (layout at mla_plan_splits): E entries (E = units + R
- * for the balanced policy, R x the uniform split count for the uniform one;
- * units = num_ctas / ceil(M / row block), row block 32 for M <= 32 else 64),
- * two job counters, 2E range words and 8 x units unit-table words. Returns
- * the length or a negative mla_status. Host only; launches nothing. */
+ * fills for this shape (layout at mla_plan_splits): E entries (E = units +
+ * R*groups for the balanced policy, R*groups x the uniform split count for the
+ * uniform one; units = max(1, num_ctas / ceil(Mg / row block)), Mg = (k /
+ * groups) * H rows per row group, row block 32 for Mg <= 32 else 64), two job
+ * counters, 2E range words and 8 x units unit-table words. Returns the length
+ * or a negative mla_status. Host only; launches nothing. */
 int32_t mla_plan_list_len(const mla_shape *shape);
 
 /* Bytes of split-KV workspace mla_folded_decode and mla_split_combine need for
