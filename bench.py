@@ -489,48 +489,96 @@ class L2Flush:
 
 def e2e_rows_per_s(batch, dev, steps):
     """The same metric through the public API with HOST buffers: every step
-    copies the inputs from pinned host memory, decodes, and reads the outputs
-    back into pinned host memory."""
+    copies its inputs from pinned host memory, plans, decodes and reads out
+    and lse back into pinned host memory; every byte crosses the host link
+    inside the timed region.
+
+    Returns (pipelined rows/s, serial rows/s, H2D bytes, D2H bytes). Serial:
+    one stream, copy -> plan -> decode -> read-back, step after step.
+    Pipelined: two sets of device buffers, the copies on their own streams,
+    so that step i+1's inputs stream in while step i computes and step i-1's
+    outputs stream back, as a serving loop overlaps them; the host-to-device
+    link then sets the pace."""
     import mla_decode_attention_folded_gb300 as mla
     hq, hkv = batch.q.pin_memory(), batch.kv.pin_memory()
     hbt, hlens = batch.block_table.pin_memory(), batch.seq_lens.pin_memory()
     R, M = batch.R, batch.M
-    hout = torch.empty((R, M, 512), dtype=torch.bfloat16).pin_memory()
-    hlse = torch.empty((R, M), dtype=torch.float32).pin_memory()
-    q = torch.empty_like(hq, device=dev)
-    kv = torch.empty_like(hkv, device=dev)
-    bt = torch.empty_like(hbt, device=dev)
-    lens = torch.empty_like(hlens, device=dev)
-    out = torch.empty((R, M, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((R, M), dtype=torch.float32, device=dev)
+    host_in = (hq, hkv, hbt, hlens)
+
+    def device_set():
+        return ([torch.empty_like(t, device=dev) for t in host_in],
+                torch.empty((R, M, 512), dtype=torch.bfloat16, device=dev),
+                torch.empty((R, M), dtype=torch.float32, device=dev),
+                torch.empty((R, M, 512), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((R, M), dtype=torch.float32).pin_memory())
+
+    sets = [device_set(), device_set()]
     eng = mla.FoldedMla(R, batch.k, batch.H, hbt.shape[1], hkv.shape[0], dev)
     bmm1 = float(np.float32(batch.sm_scale) * np.float32(batch.q_scale) * np.float32(batch.kv_scale))
     bmm2 = float(batch.kv_scale)
 
-    def one():
-        q.copy_(hq, non_blocking=True)
-        kv.copy_(hkv, non_blocking=True)
-        bt.copy_(hbt, non_blocking=True)
-        lens.copy_(hlens, non_blocking=True)
+    def compute(ins, out, lse):
+        q, kv, bt, lens = ins
         eng.plan(lens)
         eng.decode(q, kv, bt, lens, bmm1, bmm2, out=out, lse=lse)
+
+    def serial(i):
+        ins, out, lse, hout, hlse = sets[0]
+        for d, h in zip(ins, host_in):
+            d.copy_(h, non_blocking=True)
+        compute(ins, out, lse)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        one()
-    t1.record()
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hkv, hbt, hlens))
-    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
-    return R * batch.k / (ms / 1e3), h2d, d2h
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = [{k: torch.cuda.Event() for k in ("in", "comp", "out")} for _ in range(2)]
+    used = [False, False]
+
+    def pipelined(i):
+        b = i % 2
+        ins, out, lse, hout, hlse = sets[b]
+        e = ev[b]
+        if used[b]:
+            s_in.wait_event(e["comp"])      # step i-2 has read these inputs
+            s_comp.wait_event(e["out"])     # and its outputs are back on the host
+        with torch.cuda.stream(s_in):
+            for d, h in zip(ins, host_in):
+                d.copy_(h, non_blocking=True)
+            e["in"].record(s_in)
+        s_comp.wait_event(e["in"])
+        with torch.cuda.stream(s_comp):
+            compute(ins, out, lse)
+            e["comp"].record(s_comp)
+        s_out.wait_event(e["comp"])
+        with torch.cuda.stream(s_out):
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            e["out"].record(s_out)
+        used[b] = True
+
+    def timed(step, streams):
+        cur = torch.cuda.current_stream(dev)
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(cur)
+        for st in streams:
+            st.wait_event(t0)
+        for i in range(3, 3 + steps):
+            step(i)
+        for st in streams:
+            cur.wait_stream(st)
+        t1.record(cur)
+        torch.cuda.synchronize(dev)
+        return R * batch.k / (t0.elapsed_time(t1) / steps / 1e3)
+
+    serial_v = timed(serial, [])
+    piped_v = timed(pipelined, [s_in, s_comp, s_out])
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = R * M * 512 * 2 + R * M * 4
+    return piped_v, serial_v, h2d, d2h
 
 
 VARIANTS = (("folded_uniform", 1, True), ("unfolded_balanced", 0, False),
@@ -650,12 +698,12 @@ def run_ours(args):
                 per_workload[name] = measure_side_workload(
                     name, dev, flush, args.per_workload_steps, not args.no_variants)
 
-    e2e_v, h2d, d2h = e2e_rows_per_s(batch, dev, args.e2e_steps)
+    e2e_v, e2e_serial, h2d, d2h = e2e_rows_per_s(batch, dev, args.e2e_steps)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([e2e_v], device=dev, dtype=torch.float64)
+        t = torch.tensor([e2e_v, e2e_serial], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MIN)
-        e2e_v = float(t[0]) * world
+        e2e_v, e2e_serial = float(t[0]) * world, float(t[1]) * world
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -699,7 +747,11 @@ def run_ours(args):
                          in_chain=in_chain),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_v, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "serial_value": e2e_serial,
+                "mode": "pipelined: step i+1's host-to-device copies overlap step i's plan "
+                        "and decode and step i-1's read-back (two device buffer sets); "
+                        "serial_value runs copy, compute and read-back in order on one "
+                        "stream"},
         "gpu_launches": args.steps * main.launches,
         "clocks": clk,
         "status": status,
