@@ -556,23 +556,29 @@ def e2e_rows_per_s(batch, dev, steps):
             e["out"].record(s_out)
         used[b] = True
 
-    def timed(step, streams):
+    def timed(step, streams, reps=3):
+        """Median over `reps` timed runs of `steps` steps each (a host hiccup
+        in one run, which starves the pipelined loop, does not set the figure)."""
         cur = torch.cuda.current_stream(dev)
         for i in range(3):
             step(i)
         torch.cuda.synchronize(dev)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(cur)
-        for st in streams:
-            st.wait_event(t0)
-        for i in range(3, 3 + steps):
-            step(i)
-        for st in streams:
-            cur.wait_stream(st)
-        t1.record(cur)
-        torch.cuda.synchronize(dev)
-        return R * batch.k / (t0.elapsed_time(t1) / steps / 1e3)
+        rates, i = [], 3
+        for _ in range(reps):
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(cur)
+            for st in streams:
+                st.wait_event(t0)
+            for _ in range(steps):
+                step(i)
+                i += 1
+            for st in streams:
+                cur.wait_stream(st)
+            t1.record(cur)
+            torch.cuda.synchronize(dev)
+            rates.append(R * batch.k / (t0.elapsed_time(t1) / steps / 1e3))
+        return float(np.median(rates))
 
     serial_v = timed(serial, [])
     piped_v = timed(pipelined, [s_in, s_comp, s_out])
@@ -751,7 +757,7 @@ def run_ours(args):
                 "mode": "pipelined: step i+1's host-to-device copies overlap step i's plan "
                         "and decode and step i-1's read-back (two device buffer sets); "
                         "serial_value runs copy, compute and read-back in order on one "
-                        "stream"},
+                        "stream; each the median of three timed runs of e2e_steps steps"},
         "gpu_launches": args.steps * main.launches,
         "clocks": clk,
         "status": status,
