@@ -244,6 +244,46 @@ def test_many_splits_of_one_request():
     assert_close(out, lse, ref_o, ref_l, "many splits")
 
 
+def _random_cases(n, seed):
+    """Seeded random shapes: R, k, H, row groups, lengths (page and tile
+    edges, empty and one-key requests mixed in), policy, CTA count and split
+    limits; each case's oracle work (rows x keys) kept to a few million."""
+    rng = np.random.default_rng(seed)
+    edges = [0, 1, 63, 64, 65, 95, 96, 97, 127, 128, 129, 191, 192, 193]
+    out = []
+    while len(out) < n:
+        R = int(rng.integers(1, 10))
+        k = int(rng.integers(1, 9))
+        H = int(rng.choice([1, 2, 3, 5, 8, 16, 33, 64]))
+        lens = [int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(1, 3000))
+                for _ in range(R)]
+        if k * H * sum(lens) > 3_000_000 or max(lens) == 0:
+            continue
+        divisors = [d for d in range(1, k + 1) if k % d == 0]
+        groups = int(rng.choice(divisors))
+        policy = int(rng.choice([pl.BALANCED, pl.UNIFORM]))
+        num_ctas = int(rng.choice([1, 3, 16, 57, 152]))
+        mst = int(rng.choice([64, 256]))
+        ms = int(rng.choice([3, 64]))
+        out.append((tuple(lens), k, H, groups, policy, num_ctas, mst, ms))
+    return out
+
+
+@pytest.mark.parametrize("lens,k,H,groups,policy,G,mst,ms", _random_cases(40, 2026))
+def test_random_shapes_match_oracle(lens, k, H, groups, policy, G, mst, ms):
+    """Seeded random shapes against the oracle, element by element."""
+    b = make_batch_from_lengths(lens, k, H, seed=len(lens) * 1009 + k * 31 + H, value_std=1.0,
+                                scaling="amax", fill=-5, extra_pages=2)
+    ref_o, ref_l = oracle_full(b)
+    out, lse, status, _ = run_decode(b, policy=policy, num_ctas=G, min_split_tokens=mst,
+                                     max_splits=ms, groups=groups)
+    assert status == 0
+    assert_close(out, lse, ref_o, ref_l, f"{lens} k={k} H={H} groups={groups} G={G}")
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(out[i] == 0) and torch.all(torch.isneginf(lse[i]))
+
+
 @pytest.mark.parametrize("lens,k,H,G,groups,policy", [
     ((6000,) + (300,) * 30 + (0, 90), 4, 8, 5, 1, pl.BALANCED),   # 32-row kernel, an empty request
     ((4000, 2500) + (700,) * 12, 7, 8, 7, 1, pl.BALANCED),       # 64-row kernel
