@@ -77,6 +77,40 @@ def test_decode_uv_matches_oracle(lens, k, H, groups):
     _check(y, ref_y, o_ref, w, lambda a: ATOL + (RTOL + EPS) * a, f"lens={lens} k={k} H={H}")
 
 
+def _random_uv_cases(n, seed):
+    """Seeded random shapes for the fused reducer: tokens per row block
+    (k / groups), heads, lengths at page and tile edges, empty requests."""
+    rng = np.random.default_rng(seed)
+    edges = [0, 1, 63, 64, 65, 127, 128, 129]
+    out = []
+    while len(out) < n:
+        R = int(rng.integers(1, 8))
+        k = int(rng.integers(1, 9))
+        H = int(rng.choice([1, 2, 4, 8, 16, 64]))
+        lens = [int(rng.choice(edges)) if rng.random() < 0.3 else int(rng.integers(1, 3500))
+                for _ in range(R)]
+        if k * H * sum(lens) > 2_000_000 or max(lens) == 0:
+            continue
+        groups = int(rng.choice([d for d in range(1, k + 1) if k % d == 0]))
+        out.append((tuple(lens), k, H, groups))
+    return out
+
+
+@pytest.mark.parametrize("lens,k,H,groups", _random_uv_cases(12, 2027))
+def test_random_shapes_uv_match_oracle(lens, k, H, groups):
+    """Decode + fused W_UV reduction on seeded random shapes against the
+    oracle's exact product, with the end-to-end bound of the module docstring."""
+    b = make_batch_from_lengths(lens, k, H, seed=len(lens) * 101 + k * 7 + H, scaling="amax")
+    w, w_dev = _w_views(H, seed=k + H)
+    y, status, _ = _decode_uv(b, w_dev, groups=groups, min_split_tokens=64)
+    assert status == 0
+    ref_o, _ = oracle_full(b)
+    o_ref = ref_o.reshape(b.R * b.k, b.H, 512)
+    ref_y = ouv.uv_project(o_ref, w)
+    _check(y, ref_y, o_ref, w, lambda a: ATOL + (RTOL + EPS) * a,
+           f"lens={lens} k={k} H={H} groups={groups}")
+
+
 def test_uv_on_oracle_partials():
     """The fused reducer alone, on split partials and one-split rows the oracle
     made over the planned splits."""
